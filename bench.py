@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark of the block-sparse prefill attention path on GB300.
+
+One step = one pass of the whole hot path over one layer of synthetic input:
+fp_discover (K/V block means + block-score map) -> fp_select (threshold,
+sink/local, CSR) -> fp_sparse_attn (paged, PackGQA, mean correction), each a
+C-ABI call into libfprefill.
+
+Default workload: the Qwen3-30B-A3B-shaped layer at 128K (batch 1,
+L = 131072, 32 query / 4 kv heads, d = 128, 64-token shuffled pages, bf16,
+alpha = 0.1, mean correction on), inputs from the seeded generator.  The
+headline value is dense-equivalent TFLOP/s = 4 * d * H_q * (causal query-key
+pairs) / (ms per layer); ms per layer is reported beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With --gpus N > 1 (under torchrun) every rank runs an independent replica of
+the layer (the path has no exchange step): weak scaling, value = the work of
+all ranks / the slowest rank's time.  --impl reference times the float64 CPU
+oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse prefill attn ms/layer + dense-equiv TFLOP/s at 128K BF16/FP8, 1×GB300"
+UNIT = "TFLOP/s (dense-equivalent)"
+
+
+# ----------------------------------------------------------------------------
+# workload arithmetic
+# ----------------------------------------------------------------------------
+
+def causal_pairs(spec) -> int:
+    return sum(lq * s + lq * (lq + 1) // 2 for lq, s in spec.requests)
+
+
+def dense_equiv_flop(spec) -> float:
+    return 4.0 * spec.d * spec.h_q * causal_pairs(spec)
+
+
+def index_stats(spec, row_ptr: np.ndarray):
+    """Kept blocks per row -> density over causal (I, J) pairs, the executed
+    tile FLOPs of the attention kernel and its algorithmic FLOPs."""
+    counts = np.diff(row_ptr.astype(np.int64))
+    g = spec.h_q // spec.h_kv
+    Is, rows = [], 0
+    for lq, s in spec.requests:
+        nqb = -(-lq // 128)
+        I = s // 128 + np.arange(nqb)
+        Is.append(np.repeat(I, spec.h_kv))
+        rows += nqb * spec.h_kv
+    I = np.concatenate(Is)
+    causal = (I + 1).sum()
+    kept = counts.sum()
+    skipped = (I - (counts - 1)).clip(min=0)            # earlier blocks without a kept entry
+    tile = 4.0 * spec.d * 128 * 128                      # S + PV of one 128x128 tile, one head
+    kept_flop = tile * g * kept
+    corr_flop = 4.0 * spec.d * 128 * g * skipped.sum()  # one mean token per skipped block per query
+    return dict(density=float(kept / causal), nnz=int(kept), causal_pairs_blocks=int(causal),
+                kept_flop=float(kept_flop), corr_flop=float(corr_flop),
+                csr_bytes=int(4 * (len(row_ptr) + kept)))
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        exe = shutil.which("nvidia-smi")
+        if exe:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen([exe, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def cuda_time(fn, steps, stream):
+    import torch
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def run_ours(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    from block_sparse_long_fp_gb300 import fprefill, synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    spec = synth.config_spec(args.workload)
+    t0 = time.time()
+    case = synth.make_case(spec)
+    gen_s = time.time() - t0
+    layer = fprefill.layer_from_case(case, device=dev)
+    if args.logit_scale != 1.0:
+        layer.q.mul_(args.logit_scale)          # exact for powers of two
+    stream = torch.cuda.current_stream()
+    flop = dense_equiv_flop(spec)
+
+    # --- warm-up and one index for the statistics ---
+    for _ in range(args.warmup):
+        out, _, (row_ptr, col_idx, nnz) = layer.prefill()
+    torch.cuda.synchronize()
+    status = layer.device_status()
+    stats = index_stats(spec, row_ptr.cpu().numpy())
+
+    # --- the timed region: K whole steps, barrier + sync on both sides ---
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        ms = cuda_time(lambda: layer.prefill(), args.steps, stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = clk.summary()
+
+    # --- per-stage breakdown and the attention kernel alone ---
+    k_mean, v_mean, score = layer.discover()
+    rp, ci, nz = layer.select(score)
+    reps = max(2, min(args.steps, 5))
+    ms_disc = cuda_time(lambda: layer.discover(k_mean, v_mean, score), reps, stream)
+    ms_sel = cuda_time(lambda: layer.select(score, rp, ci, nz), reps, stream)
+    out_buf = torch.empty_like(layer.q, dtype=torch.bfloat16)
+    ms_attn = cuda_time(lambda: layer.sparse_attn(rp, ci, k_mean, v_mean, out=out_buf, want_lse=False),
+                        reps, stream)
+    ms_dense = None
+    if args.dense_steps > 0:
+        layer.dense_attn(out=out_buf, want_lse=False)
+        ms_dense = cuda_time(lambda: layer.dense_attn(out=out_buf, want_lse=False), args.dense_steps, stream)
+
+    # --- end to end through the C ABI with host buffers ---
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e(layer, args.e2e_steps, flop)
+
+    peaks, peak_kind = load_peaks()
+    attn_flop = stats["kept_flop"] + stats["corr_flop"]
+    achieved = attn_flop / (ms_attn * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    value = world * flop / (ms * 1e-3) / 1e12
+    res = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded block-coherent Q/K with sink and needles, V ~ N(0,1))",
+        "config": {"workload": spec.name, "batch": spec.batch, "seq_len": spec.total_q,
+                   "h_q": spec.h_q, "h_kv": spec.h_kv, "d": spec.d, "page_size": spec.page_size,
+                   "page_layout": spec.layout, "alpha": 0.1, "sink_tokens": 256, "local_tokens": 512,
+                   "block": 128, "mean_correction": True, "logit_scale": args.logit_scale,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (Q alone is 1 GiB)"},
+        "ms_per_layer": round(ms, 4),
+        "stages_ms": {"discover": round(ms_disc, 4), "select": round(ms_sel, 4),
+                      "sparse_attn": round(ms_attn, 4)},
+        "density": round(stats["density"], 5), "nnz_blocks": stats["nnz"], "csr_bytes": stats["csr_bytes"],
+        "dense_attn_ms": None if ms_dense is None else round(ms_dense, 4),
+        "speedup_vs_own_dense": None if ms_dense is None else round(ms_dense / ms, 3),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "attn_kernel (fp_sparse_attn)",
+                     "peak_source": f"{peak_kind} bf16 sustained (MEASURED_PEAKS.json)"},
+        "gpu_launches": 8 * args.steps,
+        "device_status": status,
+        "clocks": clocks,
+        "gen_seconds": round(gen_s, 1),
+    }
+    if e2e:
+        res["e2e"] = e2e
+    return res, case
+
+
+def run_e2e(layer, steps, flop):
+    """Host pinned inputs -> device, the three C-ABI calls, output -> host."""
+    import torch
+    host = {n: getattr(layer, n).cpu().pin_memory() for n in ("q", "k_cache", "v_cache", "block_table")}
+    out_dev = torch.empty((layer.total_q, layer.h_q, 128), dtype=torch.bfloat16, device=layer.q.device)
+    out_host = torch.empty(out_dev.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for n, t in host.items():
+            getattr(layer, n).copy_(t, non_blocking=True)
+        layer.prefill(out=out_dev)
+        out_host.copy_(out_dev, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    ms = cuda_time(step, steps, stream)
+    return {"value": round(flop / (ms * 1e-3) / 1e12, 3), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ----------------------------------------------------------------------------
+# the float64 oracle on a bounded sample (CPU baseline and reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_sample(case, seconds: float, seed: int = 0):
+    """Time the oracle's full path (pool, score, select, attention) on query
+    blocks of one kv head, adding blocks until `seconds` have elapsed; scale
+    by the share of the layer's work they represent (work of a row is
+    proportional to its causal length I+1)."""
+    import oracle
+    spec = case.spec
+    r = max(range(spec.batch), key=lambda x: spec.requests[x][0])
+    lq, start = spec.requests[r]
+    hkv, g, B = spec.h_kv, spec.h_q // spec.h_kv, 128
+    nqb = -(-lq // B)
+    rng = np.random.default_rng(seed)
+    t_all = time.perf_counter()
+    k, v = oracle.request_kv(case, r)            # decode (not counted as method work)
+    t0 = time.perf_counter()
+    kbar, vbar = oracle.pool(k, B), oracle.pool(v, B)
+    t_pool = time.perf_counter() - t0
+    q0 = int(case.cu_seqlens_q[r])
+    done_w, t_rows, nblocks = 0.0, 0.0, 0
+    order = rng.permutation(nqb)
+    h = 0
+    for i in order:
+        rows = slice(i * B, min(lq, (i + 1) * B))
+        qs = oracle.decode(case.q[q0 + rows.start:q0 + rows.stop], spec.dtype) * \
+            case.q_scale.astype(np.float64)[None, :, None]
+        I = start // B + i
+        qstart = start + i * B            # the block seen as a request starting at its first query
+        t0 = time.perf_counter()
+        s = oracle.score_rows(qs, qstart, hkv, B, 1 / math.sqrt(spec.d), kbar, [h])[0]
+        keep_row, _ = oracle.select_row(s, I, 0.1, B, 256, 512)
+        keep = np.zeros((1, hkv, kbar.shape[0]), np.uint8)
+        keep[0, h, :I + 1] = keep_row
+        n = rows.stop - rows.start
+        qi = np.repeat(np.arange(n), g)
+        qh = np.tile(np.arange(h * g, (h + 1) * g), n)
+        oracle.attn_rows(qs, qstart, k, v, kbar, vbar, B, 1 / math.sqrt(spec.d), keep, True, qi, qh)
+        t_rows += time.perf_counter() - t0
+        done_w += (I + 1) * (rows.stop - rows.start)
+        nblocks += 1
+        if time.perf_counter() - t_all > seconds:
+            break
+    total_w = 0.0
+    for lq_, st_ in spec.requests:
+        total_w += hkv * sum((st_ // B + i + 1) * min(B, lq_ - i * B) for i in range(-(-lq_ // B)))
+    est_ms = (t_rows * total_w / done_w + t_pool * spec.total_k / k.shape[0]) * 1e3
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return est_ms, dict(kind="oracle", cores=threads,
+                        sample=f"{nblocks} query blocks x 1 kv head of request {r} (full pooling), "
+                               f"scaled by causal work to the whole layer",
+                        sampled_seconds=round(t_rows + t_pool, 2))
+
+
+def run_reference(args, rank, world):
+    from block_sparse_long_fp_gb300 import synth
+    spec = synth.config_spec(args.workload)
+    case = synth.make_case(spec)
+    flop = dense_equiv_flop(spec)
+    per = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for w in range(args.warmup):
+        oracle_sample(case, per, seed=100 + w)
+    times = []
+    info = None
+    for s in range(args.steps):
+        est_ms, info = oracle_sample(case, per, seed=s)
+        times.append(est_ms)
+    ms = statistics.median(times)
+    value = flop / (ms * 1e-3) / 1e12
+    info["value"] = value
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": spec.name, "batch": spec.batch, "seq_len": spec.total_q, "h_q": spec.h_q,
+                       "h_kv": spec.h_kv, "d": spec.d, "page_size": spec.page_size, "alpha": 0.1,
+                       "mean_correction": True},
+            "cpu_baseline": info,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--logit-scale", type=float, default=1.0)
+    ap.add_argument("--dense-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            import oracle
+            oracle.build()
+            print(json.dumps(run_reference(args, rank, world)))
+        return
+    from block_sparse_long_fp_gb300 import build as _b
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+        if rank == 0:
+            _b.build()
+        dist.barrier()
+    else:
+        _b.build()
+    res, case = run_ours(args, rank, world)
+    if rank == 0 and args.cpu_seconds > 0:
+        import oracle
+        oracle.build()
+        est_ms, info = oracle_sample(case, args.cpu_seconds)
+        info["value"] = round(dense_equiv_flop(case.spec) / (est_ms * 1e-3) / 1e12, 6)
+        info["unit"] = UNIT
+        info["ms_per_layer_est"] = round(est_ms, 1)
+        res["cpu_baseline"] = info
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,285 @@
+// The C ABI of libfprefill (declared in include/fprefill.h): argument
+// validation, the per-batch descriptor, workspace sizing and kernel launches.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "launch.cuh"
+
+
+using namespace fp;
+
+namespace {
+
+unsigned long long g_wait_ns = 200000000ull;    // bounded-wait limit inside kernels (200 ms)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side checks of the shape and the varlen descriptors; fills bd.
+fp_status build_desc(const fp_problem *p, const fp_params *prm, BatchDesc *bd) {
+    if (!p || !prm || !bd) return FP_ERR_INVALID;
+    if (p->batch < 1 || p->batch > FP_MAX_BATCH) return p->batch < 1 ? FP_ERR_INVALID : FP_ERR_UNSUPPORTED;
+    if (p->h_q < 1 || p->h_kv < 1 || p->h_q % p->h_kv) return FP_ERR_INVALID;
+    if (p->d != kHeadDim || prm->block != kBlock) return FP_ERR_UNSUPPORTED;
+    if (p->dtype != FP_BF16 && p->dtype != FP_E4M3) return FP_ERR_INVALID;
+    if (!p->cu_seqlens_q || !p->seqlens_k || !p->q_start_pos) return FP_ERR_INVALID;
+    if (p->cu_seqlens_q[0] != 0) return FP_ERR_INVALID;
+    if (prm->sink_tokens < 0 || prm->local_tokens < 0 || !(prm->alpha >= 0.f)) return FP_ERR_INVALID;
+    memset(bd, 0, sizeof(*bd));
+    bd->batch = p->batch;
+    bd->h_q = p->h_q;
+    bd->h_kv = p->h_kv;
+    bd->g = p->h_q / p->h_kv;
+    long long rows = 0, kb = 0, sc = 0;
+    int max_nkb = 1;
+    for (int r = 0; r < p->batch; ++r) {
+        long long lq = (long long)p->cu_seqlens_q[r + 1] - p->cu_seqlens_q[r];
+        long long start = p->q_start_pos[r];
+        long long lk = p->seqlens_k[r];
+        if (lq < 0 || start < 0 || start % kBlock || lk != start + lq) return FP_ERR_INVALID;
+        long long nqb = (lq + kBlock - 1) / kBlock, nkb = (lk + kBlock - 1) / kBlock;
+        if (nkb > FP_MAX_KEY_BLOCKS) return FP_ERR_UNSUPPORTED;
+        long long I0 = start / kBlock;
+        ReqDesc &q = bd->req[r];
+        q.q_off = p->cu_seqlens_q[r];
+        q.lq = (int)lq;
+        q.lk = (int)lk;
+        q.start = (int)start;
+        q.nqb = (int)nqb;
+        q.nkb = (int)nkb;
+        q.row_base = (int)rows;
+        q.kb_base = (int)kb;
+        q.score_base = sc;
+        rows += nqb * p->h_kv;
+        kb += nkb;
+        sc += (long long)p->h_kv * (nqb * (I0 + 1) + nqb * (nqb - 1) / 2);
+        if (nkb > max_nkb) max_nkb = (int)nkb;
+    }
+    if (rows > (1ll << 30) || kb > (1ll << 30) || p->cu_seqlens_q[p->batch] > (1 << 30)) return FP_ERR_UNSUPPORTED;
+    bd->total_q = p->cu_seqlens_q[p->batch];
+    bd->total_rows = (int)rows;
+    bd->total_kb = (int)kb;
+    bd->max_nkb = max_nkb;
+    bd->score_size = sc;
+    return FP_OK;
+}
+
+// Checks of the device operands shared by discover and the attention.
+fp_status check_kv(const fp_problem *p, const BatchDesc &bd) {
+    if (!p->k_cache || !p->v_cache || !p->block_table) return FP_ERR_INVALID;
+    if (!aligned16(p->k_cache) || !aligned16(p->v_cache)) return FP_ERR_INVALID;
+    const int ps = p->page_size;
+    if (ps < 16 || !((kBlock % ps == 0) || (ps % kBlock == 0))) return FP_ERR_UNSUPPORTED;
+    if (p->num_pages < 1) return FP_ERR_INVALID;
+    if ((long long)p->num_pages * ps > (1ll << 31) - 1) return FP_ERR_UNSUPPORTED;
+    for (int r = 0; r < bd.batch; ++r)
+        if ((bd.req[r].lk + ps - 1) / ps > p->max_pages_per_seq) return FP_ERR_INVALID;
+    if (p->dtype == FP_E4M3 && (!p->k_scale || !p->v_scale)) return FP_ERR_INVALID;
+    return FP_OK;
+}
+
+fp_status check_q(const fp_problem *p) {
+    if (!p->q || !aligned16(p->q)) return FP_ERR_INVALID;
+    const int esz = p->dtype == FP_BF16 ? 2 : 1;
+    if (p->q_stride_head < p->d || p->q_stride_tok < (long long)p->q_stride_head * (p->h_q - 1) + p->d)
+        return FP_ERR_INVALID;
+    if ((p->q_stride_head * esz) % 16 || (p->q_stride_tok * esz) % 16) return FP_ERR_INVALID;
+    if (p->dtype == FP_E4M3 && !p->q_scale) return FP_ERR_INVALID;
+    return FP_OK;
+}
+
+float softmax_scale_of(const fp_params *prm, int d) {
+    return prm->softmax_scale > 0.f ? prm->softmax_scale : 1.f / sqrtf((float)d);
+}
+
+int *status_ptr(void *ws) { return reinterpret_cast<int *>(ws); }
+
+size_t attn_ws_bytes(const BatchDesc &bd) {
+    size_t n = kWsHeaderBytes;
+    n += align_up((size_t)bd.total_rows * (bd.g / 2 > 0 ? bd.g / 2 : 1) * sizeof(int), 256);
+    n += 2 * align_up((size_t)bd.total_kb * bd.h_kv * kHeadDim * 2, 256);
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+fp_params fp_default_params(void) {
+    fp_params p;
+    p.block = 128;
+    p.sink_tokens = 256;
+    p.local_tokens = 512;
+    p.alpha = 0.1f;
+    p.softmax_scale = 0.f;
+    p.mean_correction = 1;
+    return p;
+}
+
+long long fp_num_rows(const fp_problem *p, const fp_params *prm) {
+    BatchDesc bd;
+    return build_desc(p, prm, &bd) == FP_OK ? bd.total_rows : -1;
+}
+
+long long fp_num_key_blocks(const fp_problem *p, const fp_params *prm) {
+    BatchDesc bd;
+    return build_desc(p, prm, &bd) == FP_OK ? bd.total_kb : -1;
+}
+
+long long fp_score_size(const fp_problem *p, const fp_params *prm) {
+    BatchDesc bd;
+    return build_desc(p, prm, &bd) == FP_OK ? bd.score_size : -1;
+}
+
+long long fp_total_q(const fp_problem *p) {
+    if (!p || !p->cu_seqlens_q || p->batch < 1) return -1;
+    return p->cu_seqlens_q[p->batch];
+}
+
+size_t fp_discover_workspace_size(const fp_problem *p, const fp_params *prm) {
+    (void)p;
+    (void)prm;
+    return kWsHeaderBytes;
+}
+
+fp_status fp_discover(const fp_problem *p, const fp_params *prm, float *k_mean, float *v_mean, float *score,
+                      void *ws, size_t ws_bytes, void *stream) {
+    BatchDesc bd;
+    fp_status s = build_desc(p, prm, &bd);
+    if (s != FP_OK) return s;
+    if ((s = check_kv(p, bd)) != FP_OK || (s = check_q(p)) != FP_OK) return s;
+    if (!k_mean || !v_mean || !score || !aligned16(k_mean) || !aligned16(v_mean)) return FP_ERR_INVALID;
+    if (!ws || ws_bytes < kWsHeaderBytes) return FP_ERR_WORKSPACE;
+    if (score_smem_bytes(bd.max_nkb) > 227 * 1024) return FP_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool fp8 = p->dtype == FP_E4M3;
+    if (bd.total_kb > 0 &&
+        launch_pool(bd, fp8, p->k_cache, p->v_cache, p->page_size, p->num_pages, p->block_table,
+                    p->max_pages_per_seq, p->k_scale, p->v_scale, k_mean, v_mean, status_ptr(ws), st) != cudaSuccess)
+        return FP_ERR_CUDA;
+    if (bd.total_rows > 0 &&
+        launch_score(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean, softmax_scale_of(prm, p->d),
+                     score, st) != cudaSuccess)
+        return FP_ERR_CUDA;
+    return FP_OK;
+}
+
+size_t fp_select_workspace_size(const fp_problem *p, const fp_params *prm) {
+    BatchDesc bd;
+    if (build_desc(p, prm, &bd) != FP_OK) return 0;
+    return kWsHeaderBytes + align_up((size_t)bd.total_rows * sizeof(int), 256);
+}
+
+fp_status fp_select(const fp_problem *p, const fp_params *prm, const float *score, int *row_ptr, int *col_idx,
+                    long long col_capacity, int *nnz_dev, unsigned char *dense_mask_opt, void *ws, size_t ws_bytes,
+                    void *stream) {
+    BatchDesc bd;
+    fp_status s = build_desc(p, prm, &bd);
+    if (s != FP_OK) return s;
+    if (!score || !row_ptr || !col_idx || !nnz_dev) return FP_ERR_INVALID;
+    if (col_capacity < bd.score_size) return FP_ERR_INVALID;
+    if (!ws || ws_bytes < fp_select_workspace_size(p, prm)) return FP_ERR_WORKSPACE;
+    const int sink_blocks = (prm->sink_tokens + kBlock - 1) / kBlock;
+    const int local_blocks = (prm->local_tokens + kBlock - 1) / kBlock;
+    int *counts = reinterpret_cast<int *>(static_cast<char *>(ws) + kWsHeaderBytes);
+    if (launch_select(bd, prm->alpha, sink_blocks, local_blocks, score, counts, row_ptr, col_idx, col_capacity,
+                      nnz_dev, dense_mask_opt, status_ptr(ws), (cudaStream_t)stream) != cudaSuccess)
+        return FP_ERR_CUDA;
+    return FP_OK;
+}
+
+size_t fp_attn_workspace_size(const fp_problem *p, const fp_params *prm) {
+    BatchDesc bd;
+    if (build_desc(p, prm, &bd) != FP_OK) return 0;
+    return attn_ws_bytes(bd);
+}
+
+static fp_status run_attn(const fp_problem *p, const fp_params *prm, const int *row_ptr, const int *col_idx,
+                          const float *k_mean, const float *v_mean, void *out, float *lse, void *ws, size_t ws_bytes,
+                          void *stream) {
+    BatchDesc bd;
+    fp_status s = build_desc(p, prm, &bd);
+    if (s != FP_OK) return s;
+    if ((s = check_kv(p, bd)) != FP_OK || (s = check_q(p)) != FP_OK) return s;
+    if (p->dtype != FP_BF16) return FP_ERR_UNSUPPORTED;
+    if (bd.g % 2) return FP_ERR_UNSUPPORTED;
+    if (!out || !aligned16(out)) return FP_ERR_INVALID;
+    if (!ws || ws_bytes < attn_ws_bytes(bd)) return FP_ERR_WORKSPACE;
+    char *w = static_cast<char *>(ws);
+    AttnLaunch L;
+    memset(&L, 0, sizeof(L));
+    L.bd = &bd;
+    L.q = p->q;
+    L.q_stride_tok = p->q_stride_tok;
+    L.q_stride_head = p->q_stride_head;
+    L.k_cache = p->k_cache;
+    L.v_cache = p->v_cache;
+    L.page_size = p->page_size;
+    L.num_pages = p->num_pages;
+    L.block_table = p->block_table;
+    L.max_pages = p->max_pages_per_seq;
+    L.row_ptr = row_ptr;
+    L.col_idx = col_idx;
+    L.k_mean = k_mean;
+    L.v_mean = v_mean;
+    L.mean_corr = prm->mean_correction ? 1 : 0;
+    L.softmax_scale = softmax_scale_of(prm, p->d);
+    L.out = out;
+    L.lse = lse;
+    L.status = status_ptr(ws);
+    size_t off = kWsHeaderBytes;
+    L.work = reinterpret_cast<int *>(w + off);
+    off += align_up((size_t)bd.total_rows * (bd.g / 2) * sizeof(int), 256);
+    L.km16 = reinterpret_cast<__nv_bfloat16 *>(w + off);
+    off += align_up((size_t)bd.total_kb * bd.h_kv * kHeadDim * 2, 256);
+    L.vm16 = reinterpret_cast<__nv_bfloat16 *>(w + off);
+    L.wait_ns = g_wait_ns;
+    return (fp_status)launch_attn(L, (cudaStream_t)stream);
+}
+
+fp_status fp_sparse_attn(const fp_problem *p, const fp_params *prm, const int *row_ptr, const int *col_idx,
+                         const float *k_mean, const float *v_mean, void *out, float *lse_opt, void *ws,
+                         size_t ws_bytes, void *stream) {
+    if (!row_ptr || !col_idx) return FP_ERR_INVALID;
+    if (prm && prm->mean_correction && (!k_mean || !v_mean)) return FP_ERR_INVALID;
+    return run_attn(p, prm, row_ptr, col_idx, k_mean, v_mean, out, lse_opt, ws, ws_bytes, stream);
+}
+
+fp_status fp_dense_attn(const fp_problem *p, const fp_params *prm, void *out, float *lse_opt, void *ws,
+                        size_t ws_bytes, void *stream) {
+    return run_attn(p, prm, nullptr, nullptr, nullptr, nullptr, out, lse_opt, ws, ws_bytes, stream);
+}
+
+fp_status fp_reset_status(void *ws, void *stream) {
+    if (!ws) return FP_ERR_INVALID;
+    return cudaMemsetAsync(ws, 0, kWsHeaderBytes, (cudaStream_t)stream) == cudaSuccess ? FP_OK : FP_ERR_CUDA;
+}
+
+fp_status fp_device_status(const void *ws, void *stream, int *device_status) {
+    if (!ws || !device_status) return FP_ERR_INVALID;
+    int v = 0;
+    if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
+        return FP_ERR_CUDA;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FP_ERR_CUDA;
+    *device_status = v;
+    return FP_OK;
+}
+
+const char *fp_status_string(fp_status s) {
+    switch (s) {
+        case FP_OK: return "ok";
+        case FP_ERR_INVALID: return "invalid argument";
+        case FP_ERR_UNSUPPORTED: return "unsupported shape or option";
+        case FP_ERR_WORKSPACE: return "workspace missing or too small";
+        case FP_ERR_CUDA: return "CUDA runtime error";
+        case FP_ERR_DEVICE_BOUNDS: return "page-table entry out of range (device)";
+        case FP_ERR_TIMEOUT: return "bounded wait timed out (device)";
+    }
+    return "unknown status";
+}
+
+void fp_set_wait_limit_ns(unsigned long long ns) { g_wait_ns = ns ? ns : 200000000ull; }
+
+}  // extern "C"

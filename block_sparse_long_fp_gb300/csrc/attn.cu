@@ -1,0 +1,554 @@
+// Block-sparse causal attention with block-mean correction on tcgen05 (sm_103a).
+//
+// What it computes: the sparse attention of the FlashPrefill V2 paper reading,
+// section 4.1 -- kept key blocks exactly, every skipped earlier block J < I as
+// one "mean token" (kmean_J, vmean_J) of weight n_J (the V2 popular article:
+// "multiplied by the number of tokens the block originally had") -- over a
+// paged KV cache (V2 section 4.3: the address of a key is the page-table entry
+// of its page plus its offset in the page, fetched asynchronously), with the
+// g query heads of a kv group packed so that each kept KV tile is fetched once
+// for the group (PackGQA, V2 section 4.2 (1)).
+//
+// How (sm_103a design, not the Hopper one of the pages):
+//  * one CTA = one work unit = (index row (request, query block I, kv head h),
+//    a pair of query heads of the group): two 128-query tiles Q0, Q1;
+//  * warp 0 issues TMA loads (Q once; K and V tiles through the page table
+//    into a two-stage ring each; mean tiles from the bf16 copies of the block
+//    means);
+//  * warp 1 issues tcgen05 MMAs: S_t = Q_t K^T into TMEM, then O_t += P_t V
+//    with P_t read from TMEM (it overwrites S_t as packed bf16);
+//  * warps 2-5 / 6-9 are the softmax warpgroups of tile 0 / tile 1: they read
+//    S from TMEM, apply the causal mask or the mean-token bias log2(n_J),
+//    keep the running max (rescaling O in TMEM only when the max grows by
+//    more than 2^8) and write P back to TMEM;
+//  * the MMA issue order S0(j) S1(j) PV0(j) S0(j+1) PV1(j) S1(j+1) ... lets
+//    one tile's softmax overlap the other tile's MMAs (the pingpong of V2
+//    section 4.2 (3), with TMEM accumulators instead of registers);
+//  * item list of a unit: the kept blocks (CSR row, ascending), then the
+//    128-wide tiles of block means that contain at least one skipped block;
+//    the dense path walks J = 0..I with no mean tiles.
+// Every mbarrier wait is bounded (status FP_ERR_TIMEOUT instead of a hang).
+#include "common.cuh"
+#include "sm100.cuh"
+#include "launch.cuh"
+
+namespace fp {
+
+using namespace sm100;
+
+constexpr int kAttnThreads = 320;
+constexpr int kTileBytes = kBlock * kHeadDim * 2;          // 32 KB: one 128 x 128 bf16 tile
+constexpr int kHalfBytes = kTileBytes / 2;                 // 64 columns of d
+constexpr int kSmemQ = 0;
+constexpr int kSmemK = 2 * kTileBytes;
+constexpr int kSmemV = 4 * kTileBytes;
+constexpr int kSmemCtl = 6 * kTileBytes;                   // 192 KB
+constexpr int kBitmapWords = FP_MAX_KEY_BLOCKS / 32;
+constexpr int kMaxCorrTiles = FP_MAX_KEY_BLOCKS / kBlock;
+constexpr int kSmemAttn = kSmemCtl + 256 + kBitmapWords * 4 + kMaxCorrTiles * 4 + 1024;
+
+enum { BAR_Q = 0, BAR_KF = 1, BAR_KE = 3, BAR_VF = 5, BAR_VE = 7, BAR_SF = 9, BAR_PF = 11, BAR_OF = 13,
+       NUM_BARS = 15 };
+
+struct AttnArgs {
+    const int *row_ptr;       // null in dense mode
+    const int *col_idx;
+    const int *work;          // unit ids sorted by decreasing work
+    const int *block_table;
+    int max_pages;
+    int page_size;
+    int num_pages;
+    int n_pairs;              // query-head pairs per kv head
+    int mean_corr;
+    float scale_log2;         // softmax scale * log2(e)
+    __nv_bfloat16 *out;
+    float *lse;
+    int *status;
+    unsigned long long wait_ns;
+};
+
+// 128 bytes of P (64 packed bf16 pairs) -> bf16x2 word
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__global__ void __maxnreg__(200)
+attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtensorMap tmQ,
+            const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+            const __grid_constant__ CUtensorMap tmKm, const __grid_constant__ CUtensorMap tmVm,
+            const AttnArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmemCtl);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kSmemCtl + NUM_BARS * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kSmemCtl + NUM_BARS * 8 + 4);
+    int *n_corr_s = reinterpret_cast<int *>(smem + kSmemCtl + NUM_BARS * 8 + 8);
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem + kSmemCtl + 256);
+    int *corr_list = reinterpret_cast<int *>(smem + kSmemCtl + 256 + kBitmapWords * 4);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int k) { return smem_u32(&bars[k]); };
+
+    // ---- the unit ------------------------------------------------------------
+    const int unit = a.work[blockIdx.x];
+    const int row = unit / a.n_pairs;
+    const int pair = unit % a.n_pairs;
+    const int r = req_of_row(bd, row);
+    const ReqDesc &rq = bd.req[r];
+    const int local = row - rq.row_base;
+    const int il = local / bd.h_kv;
+    const int h = local % bd.h_kv;
+    const int I = rq.start / kBlock + il;
+    const int hq0 = h * bd.g + 2 * pair;
+    const bool sparse = a.row_ptr != nullptr;
+    const int rp0 = sparse ? a.row_ptr[row] : 0;
+    const int n_kept = sparse ? a.row_ptr[row + 1] - rp0 : I + 1;
+
+    // ---- set-up ----------------------------------------------------------------
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < NUM_BARS; ++k) {
+            uint32_t cnt = (k == BAR_PF || k == BAR_PF + 1) ? 128u : 1u;
+            mbar_init(bar(k), cnt);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async();
+    }
+    if (warp == 0) {
+        // kept-block bitmap and the list of mean tiles holding a skipped block
+        int n_corr = 0;
+        if (sparse && a.mean_corr && I > 0) {
+            const int nw = (I + 31) / 32;
+            for (int w = lane; w < nw; w += 32) bitmap[w] = 0u;
+            __syncwarp();
+            for (int k = lane; k < n_kept; k += 32) {
+                int J = __ldg(a.col_idx + rp0 + k);
+                if (J >= 0 && J < I) atomicOr(&bitmap[J >> 5], 1u << (J & 31));
+            }
+            __syncwarp();
+            const int ntiles = (I + kBlock - 1) / kBlock;
+            for (int c0 = 0; c0 < ntiles; c0 += 32) {
+                int c = c0 + lane;
+                bool any = false;
+                if (c < ntiles) {
+                    for (int w = 0; w < 4; ++w) {
+                        int J0 = c * kBlock + w * 32;
+                        if (J0 >= I) break;
+                        uint32_t valid = (I - J0 >= 32) ? 0xffffffffu : ((1u << (I - J0)) - 1u);
+                        if (~bitmap[J0 >> 5] & valid) any = true;
+                    }
+                }
+                unsigned m = __ballot_sync(0xffffffffu, any);
+                if (any) corr_list[n_corr + __popc(m & ((1u << lane) - 1u))] = c;
+                n_corr += __popc(m);
+            }
+        }
+        if (lane == 0) *n_corr_s = n_corr;
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int n_items = n_kept + *n_corr_s;
+    // a CTA of this launch (or an earlier one on this workspace) timed out:
+    // do no work, so a broken launch ends in one wait limit, not one per CTA
+    const bool dead = a.status && *reinterpret_cast<volatile int *>(a.status) == FP_ERR_TIMEOUT;
+
+    if (dead) {
+    } else if (n_items > 0) {
+        if (warp == 0) {
+            // ================= TMA producer =================
+            if (lane == 0) {
+                tma_prefetch_desc(&tmQ);
+                tma_prefetch_desc(&tmK);
+                tma_prefetch_desc(&tmV);
+                const int q_row0 = rq.q_off + il * kBlock;
+                mbar_expect_tx(bar(BAR_Q), 2 * kTileBytes);
+                for (int t = 0; t < 2; ++t)
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_load_3d(sbase + kSmemQ + t * kTileBytes + hf * kHalfBytes, &tmQ, bar(BAR_Q),
+                                    hf * 64, hq0 + t, q_row0);
+                const int rpb = a.page_size < kBlock ? a.page_size : kBlock;   // rows per box
+                const int oob = a.num_pages * a.page_size;                     // zero-filled rows
+                const int *bt = a.block_table + (long long)r * a.max_pages;
+                const int npages_req = (rq.lk + a.page_size - 1) / a.page_size;
+                for (int j = 0; j < n_items; ++j) {
+                    const int s = j & 1, ph = (j >> 1) & 1;
+                    const bool kept = j < n_kept;
+                    int J = 0, c = 0;
+                    if (kept) J = sparse ? __ldg(a.col_idx + rp0 + j) : j;
+                    else c = corr_list[j - n_kept];
+                    for (int op = 0; op < 2; ++op) {       // 0: K tile, 1: V tile
+                        const uint32_t full = bar(op == 0 ? BAR_KF + s : BAR_VF + s);
+                        if (j >= 2 && !mbar_wait(bar(op == 0 ? BAR_KE + s : BAR_VE + s), ph ^ 1, abort_flag,
+                                                 a.status, a.wait_ns))
+                            goto producer_done;
+                        const uint32_t dst = sbase + (op == 0 ? kSmemK : kSmemV) + s * kTileBytes;
+                        mbar_expect_tx(full, kTileBytes);
+                        if (kept) {
+                            const CUtensorMap *tm = op == 0 ? &tmK : &tmV;
+                            for (int sub = 0; sub < kBlock / rpb; ++sub) {
+                                const int tok = J * kBlock + sub * rpb;
+                                int z = oob;
+                                const int lp = tok / a.page_size;
+                                if (tok < rq.lk && lp < npages_req) {
+                                    const int pg = __ldg(bt + lp);
+                                    if (pg >= 0 && pg < a.num_pages) z = pg * a.page_size + tok % a.page_size;
+                                    else set_status(a.status, FP_ERR_DEVICE_BOUNDS);
+                                }
+                                for (int hf = 0; hf < 2; ++hf)
+                                    tma_load_3d(dst + hf * kHalfBytes + sub * rpb * 128, tm, full, hf * 64, h, z);
+                            }
+                        } else {
+                            const CUtensorMap *tm = op == 0 ? &tmKm : &tmVm;
+                            for (int hf = 0; hf < 2; ++hf)
+                                tma_load_3d(dst + hf * kHalfBytes, tm, full, hf * 64, h, rq.kb_base + c * kBlock);
+                        }
+                    }
+                }
+            producer_done:;
+            }
+        } else if (warp == 1) {
+            // ================= MMA issuer =================
+            if (lane == 0) {
+                constexpr uint32_t idS = idesc_bf16(128, 128, false);
+                constexpr uint32_t idPV = idesc_bf16(128, 128, true);
+                auto issue_S = [&](int t, int s) {
+                    const uint32_t qa = sbase + kSmemQ + t * kTileBytes;
+                    const uint32_t kb = sbase + kSmemK + s * kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                        mma_ss(tmem + t * 256, smem_desc_sw128(qa + off, 16, 1024),
+                               smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0);
+                    }
+                };
+                auto issue_PV = [&](int t, int s, bool acc) {
+                    const uint32_t vb = sbase + kSmemV + s * kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBlock / 16; ++kk)
+                        mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8,
+                               smem_desc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024), idPV, (acc || kk > 0));
+                };
+                if (!mbar_wait(bar(BAR_Q), 0, abort_flag, a.status, a.wait_ns)) goto mma_done;
+                if (!mbar_wait(bar(BAR_KF), 0, abort_flag, a.status, a.wait_ns)) goto mma_done;
+                tc_fence_after();
+                issue_S(0, 0);
+                tc_commit(bar(BAR_SF + 0));
+                issue_S(1, 0);
+                tc_commit(bar(BAR_SF + 1));
+                tc_commit(bar(BAR_KE + 0));
+                for (int j = 0; j < n_items; ++j) {
+                    const int s = j & 1, ph = (j >> 1) & 1;
+                    const int s1 = (j + 1) & 1, ph1 = ((j + 1) >> 1) & 1;
+                    const bool more = j + 1 < n_items;
+                    if (!mbar_wait(bar(BAR_VF + s), ph, abort_flag, a.status, a.wait_ns)) goto mma_done;
+                    if (!mbar_wait(bar(BAR_PF + 0), j & 1, abort_flag, a.status, a.wait_ns)) goto mma_done;
+                    tc_fence_after();
+                    issue_PV(0, s, j > 0);
+                    if (more) {
+                        if (!mbar_wait(bar(BAR_KF + s1), ph1, abort_flag, a.status, a.wait_ns)) goto mma_done;
+                        tc_fence_after();
+                        issue_S(0, s1);
+                        tc_commit(bar(BAR_SF + 0));
+                    } else {
+                        tc_commit(bar(BAR_OF + 0));
+                    }
+                    if (!mbar_wait(bar(BAR_PF + 1), j & 1, abort_flag, a.status, a.wait_ns)) goto mma_done;
+                    tc_fence_after();
+                    issue_PV(1, s, j > 0);
+                    tc_commit(bar(BAR_VE + s));
+                    if (more) {
+                        issue_S(1, s1);
+                        tc_commit(bar(BAR_SF + 1));
+                        tc_commit(bar(BAR_KE + s1));
+                    } else {
+                        tc_commit(bar(BAR_OF + 1));
+                    }
+                }
+            mma_done:;
+            }
+        } else {
+            // ================= softmax warpgroups =================
+            const int t = (warp - 2) / 4;                 // tile
+            const int quarter = warp % 4;                 // TMEM lane quarter of this warp
+            const int rowt = quarter * 32 + lane;         // row of the tile
+            const int qi = il * kBlock + rowt;            // query index inside the request
+            const int pos = rq.start + qi;                // absolute position
+            const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+            const uint32_t tS = lane_base + t * 256;
+            const uint32_t tO = tS + 128;
+            float m = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int j = 0; j < n_items && ok; ++j) {
+                const bool got = mbar_wait(bar(BAR_SF + t), j & 1, abort_flag, a.status, a.wait_ns);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }   // tcgen05.ld needs the whole warp
+                tc_fence_after();
+                uint32_t v[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, v[c]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) reg_fence(v[c]);
+                float x[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]) * a.scale_log2;
+                if (j < n_kept) {
+                    const int J = sparse ? __ldg(a.col_idx + rp0 + j) : j;
+                    const int k0 = J * kBlock;
+                    if (k0 + kBlock - 1 > pos) {          // the diagonal block: causal mask
+#pragma unroll
+                        for (int e = 0; e < 128; ++e)
+                            if (k0 + e > pos) x[e] = -INFINITY;
+                    }
+                } else {
+                    // mean tile c covers blocks 128c .. 128c+127; a skipped block J < I
+                    // is full (only the request's last block can be short, and
+                    // it is never before I), so its weight is n_J = 128: bias log2(128)
+                    const int c = corr_list[j - n_kept];
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int J0 = c * kBlock + 32 * k;
+                        uint32_t valid = J0 >= I ? 0u : (I - J0 >= 32 ? 0xffffffffu : ((1u << (I - J0)) - 1u));
+                        w[k] = valid ? (~bitmap[J0 >> 5] & valid) : 0u;   // 1 = skipped, before I
+                    }
+#pragma unroll
+                    for (int e = 0; e < 128; ++e)
+                        x[e] = ((w[e >> 5] >> (e & 31)) & 1u) ? x[e] + 7.f : -INFINITY;
+                }
+                float mx = x[0];
+#pragma unroll
+                for (int e = 1; e < 128; ++e) mx = fmaxf(mx, x[e]);
+                // grow the running max only when it rises by more than 2^8 (rarely);
+                // O is rescaled after P is written (x is dead by then), and the
+                // TMEM round trip runs warp-wide
+                const bool grow = mx > m + 8.f;
+                const bool any_grow = __any_sync(0xffffffffu, grow);
+                const float f = grow ? fast_exp2(m - mx) : 1.f;   // 0 when m = -inf
+                if (grow) {
+                    l *= f;
+                    m = mx;
+                }
+                const float ms = m == -INFINITY ? 0.f : m;
+                float rs = 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float p0 = fast_exp2(x[64 * half + 2 * e] - ms);
+                        const float p1 = fast_exp2(x[64 * half + 2 * e + 1] - ms);
+                        rs += p0 + p1;
+                        pk[e] = pack_bf16(p0, p1);
+                    }
+                    tmem_st32(tS + 32 * half, pk);
+                }
+                l += rs;
+                if (any_grow && j > 0) {
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
+                        tmem_ld_wait();
+                        reg_fence(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                        tmem_st32(tO + c * 32, o);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(BAR_PF + t));
+            }
+            // epilogue: O / l -> bf16, LSE
+            const int head = hq0 + t;
+            const bool valid = qi < rq.lq;
+            const bool fin = ok && mbar_wait(bar(BAR_OF + t), 0, abort_flag, a.status, a.wait_ns);
+            if (__all_sync(0xffffffffu, fin)) {
+                tc_fence_after();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                __nv_bfloat16 *dst = a.out + ((long long)(rq.q_off + qi) * bd.h_q + head) * kHeadDim;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_ld_wait();
+                    reg_fence(o);
+                    if (valid) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8) {
+                            uint4 w;
+                            w.x = pack_bf16(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
+                            w.y = pack_bf16(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                            w.z = pack_bf16(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                            w.w = pack_bf16(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
+                        }
+                    }
+                }
+                if (valid && a.lse)
+                    a.lse[(long long)head * bd.total_q + rq.q_off + qi] =
+                        l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+            }
+        }
+    } else if (warp >= 2) {
+        // a row with no term at all: O = 0, LSE = -inf
+        const int t = (warp - 2) / 4;
+        const int rowt = (warp % 4) * 32 + lane;
+        const int qi = il * kBlock + rowt;
+        if (qi < rq.lq) {
+            const int head = hq0 + t;
+            __nv_bfloat16 *dst = a.out + ((long long)(rq.q_off + qi) * bd.h_q + head) * kHeadDim;
+            for (int c = 0; c < kHeadDim; c += 8) *reinterpret_cast<uint4 *>(dst + c) = make_uint4(0, 0, 0, 0);
+            if (a.lse) a.lse[(long long)head * bd.total_q + rq.q_off + qi] = -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// schedule: units sorted by decreasing work (kept blocks + mean tiles), so the
+// longest rows start first and the tail of the grid is short rows (the
+// kept-count load balancing of the V2 popular article, "KV split").
+// ---------------------------------------------------------------------------
+constexpr int kSchedBins = 4096;
+
+__global__ void __launch_bounds__(1024)
+sched_kernel(const __grid_constant__ BatchDesc bd, const int *__restrict__ row_ptr, int n_pairs,
+             int mean_corr, int *__restrict__ work) {
+    __shared__ int hist[kSchedBins];
+    for (int k = threadIdx.x; k < kSchedBins; k += 1024) hist[k] = 0;
+    __syncthreads();
+    auto cost = [&](int row) {
+        const int r = req_of_row(bd, row);
+        const ReqDesc &rq = bd.req[r];
+        const int I = rq.start / kBlock + (row - rq.row_base) / bd.h_kv;
+        int c = row_ptr ? row_ptr[row + 1] - row_ptr[row] + (mean_corr ? (I + kBlock - 1) / kBlock : 0) : I + 1;
+        return min(c, kSchedBins - 1);
+    };
+    for (int row = threadIdx.x; row < bd.total_rows; row += 1024) atomicAdd(&hist[cost(row)], 1);
+    __syncthreads();
+    if (threadIdx.x == 0) {        // descending exclusive scan (4096 bins, once)
+        int run = 0;
+        for (int k = kSchedBins - 1; k >= 0; --k) {
+            int v = hist[k];
+            hist[k] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    for (int row = threadIdx.x; row < bd.total_rows; row += 1024) {
+        int slot = atomicAdd(&hist[cost(row)], 1);
+        for (int p = 0; p < n_pairs; ++p) work[slot * n_pairs + p] = row * n_pairs + p;
+    }
+}
+
+// fp32 block means -> bf16 operands of the mean tiles
+__global__ void to_bf16_kernel(const float *__restrict__ a, const float *__restrict__ b,
+                               __nv_bfloat16 *__restrict__ ao, __nv_bfloat16 *__restrict__ bo, long long n) {
+    for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n; k += (long long)gridDim.x * blockDim.x) {
+        ao[k] = __float2bfloat16_rn(a[k]);
+        bo[k] = __float2bfloat16_rn(b[k]);
+    }
+}
+
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    }
+    return fn;
+}
+
+// 3-D bf16 map over [n2][n1][128] with strides (in elements) s1, s2; box
+// (64, 1, box2), 128-byte swizzle, zero fill out of bounds.
+static bool make_map(CUtensorMap *m, const void *base, long long n1, long long n2, long long s1, long long s2,
+                     int box2) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)n1, (cuuint64_t)n2};
+    cuuint64_t strides[2] = {(cuuint64_t)(s1 * 2), (cuuint64_t)(s2 * 2)};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box2};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int attn_smem_bytes() { return kSmemAttn; }
+
+// returns 0 on success, otherwise an fp_status
+int launch_attn(const AttnLaunch &L, cudaStream_t st) {
+    const BatchDesc &bd = *L.bd;
+    const int n_pairs = bd.g / 2;
+    const bool sparse = L.row_ptr != nullptr;
+    const int units = bd.total_rows * n_pairs;
+    if (units == 0) return FP_OK;
+    const int rpb = L.page_size < kBlock ? L.page_size : kBlock;
+    CUtensorMap tmQ, tmK, tmV, tmKm, tmVm;
+    const long long total_q = bd.total_q;
+    const long long tokens = (long long)L.num_pages * L.page_size;
+    if (!make_map(&tmQ, L.q, bd.h_q, total_q, L.q_stride_head, L.q_stride_tok, kBlock)) return FP_ERR_CUDA;
+    if (!make_map(&tmK, L.k_cache, bd.h_kv, tokens, kHeadDim, (long long)bd.h_kv * kHeadDim, rpb)) return FP_ERR_CUDA;
+    if (!make_map(&tmV, L.v_cache, bd.h_kv, tokens, kHeadDim, (long long)bd.h_kv * kHeadDim, rpb)) return FP_ERR_CUDA;
+    const bool use_means = sparse && L.mean_corr;
+    if (use_means) {
+        const long long n = (long long)bd.total_kb * bd.h_kv * kHeadDim;
+        to_bf16_kernel<<<1024, 256, 0, st>>>(L.k_mean, L.v_mean, L.km16, L.vm16, n);
+        if (!make_map(&tmKm, L.km16, bd.h_kv, bd.total_kb, kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock))
+            return FP_ERR_CUDA;
+        if (!make_map(&tmVm, L.vm16, bd.h_kv, bd.total_kb, kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock))
+            return FP_ERR_CUDA;
+    } else {
+        tmKm = tmK;     // never read
+        tmVm = tmV;
+    }
+    sched_kernel<<<1, 1024, 0, st>>>(bd, L.row_ptr, n_pairs, use_means ? 1 : 0, L.work);
+    AttnArgs a;
+    a.row_ptr = L.row_ptr;
+    a.col_idx = L.col_idx;
+    a.work = L.work;
+    a.block_table = L.block_table;
+    a.max_pages = L.max_pages;
+    a.page_size = L.page_size;
+    a.num_pages = L.num_pages;
+    a.n_pairs = n_pairs;
+    a.mean_corr = use_means ? 1 : 0;
+    a.scale_log2 = L.softmax_scale * 1.4426950408889634f;
+    a.out = (__nv_bfloat16 *)L.out;
+    a.lse = L.lse;
+    a.status = L.status;
+    a.wait_ns = L.wait_ns;
+    if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttn) != cudaSuccess)
+        return FP_ERR_CUDA;
+    attn_kernel<<<units, kAttnThreads, kSmemAttn, st>>>(bd, tmQ, tmK, tmV, tmKm, tmVm, a);
+    return cudaGetLastError() == cudaSuccess ? FP_OK : FP_ERR_CUDA;
+}
+
+}  // namespace fp

@@ -1,0 +1,39 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace fp {
+cudaError_t launch_pool(const BatchDesc &bd, bool fp8, const void *k_cache, const void *v_cache, int page_size,
+                        int num_pages, const int *block_table, int max_pages, const float *k_scale,
+                        const float *v_scale, float *k_mean, float *v_mean, int *status, cudaStream_t st);
+cudaError_t launch_score(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
+                         long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
+                         float *score, cudaStream_t st);
+cudaError_t launch_select(const BatchDesc &bd, float alpha, int sink_blocks, int local_blocks, const float *score,
+                          int *counts, int *row_ptr, int *col_idx, long long col_capacity, int *nnz,
+                          unsigned char *dense_mask, int *status, cudaStream_t st);
+size_t score_smem_bytes(int max_nkb);
+
+struct AttnLaunch {
+    const BatchDesc *bd;
+    const void *q;
+    long long q_stride_tok, q_stride_head;
+    const void *k_cache, *v_cache;
+    int page_size, num_pages;
+    const int *block_table;
+    int max_pages;
+    const int *row_ptr, *col_idx;
+    const float *k_mean, *v_mean;
+    int mean_corr;
+    float softmax_scale;
+    void *out;
+    float *lse;
+    int *status;
+    int *work;
+    __nv_bfloat16 *km16, *vm16;
+    unsigned long long wait_ns;
+};
+int launch_attn(const AttnLaunch &L, cudaStream_t st);
+int attn_smem_bytes();
+}  // namespace fp

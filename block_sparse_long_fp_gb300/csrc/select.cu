@@ -1,0 +1,140 @@
+// fp_select kernels: the max-based dynamic threshold with the sink / local
+// safety net (FlashPrefill V1 summary, section 3.2; V2 paper reading, section
+// 4: 256 sink tokens, 512 local tokens, alpha = 0.1) and the compaction of the
+// kept key blocks into a CSR index (V1 section 3.3 "index-driven physical
+// jump"; V2 section 4 CSR output).
+//
+// Three launches, no host synchronisation: (1) one warp per row decides and
+// counts, (2) one CTA scans the counts into row_ptr, (3) one warp per row
+// repeats the identical decision and writes its kept blocks at row_ptr[row].
+#include "common.cuh"
+#include "launch.cuh"
+
+namespace fp {
+
+struct SelectArgs {
+    float alpha;
+    int sink_blocks;
+    int local_blocks;
+};
+
+// Row maximum of a score row, reduced across the warp in a fixed order.
+__device__ __forceinline__ float warp_row_max(const float *s, int n, int lane) {
+    float mx = -INFINITY;
+    for (int c = lane; c < n; c += 32) mx = fmaxf(mx, s[c]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    return mx;
+}
+
+__device__ __forceinline__ bool keep_block(float s, float thr, int J, int I, const SelectArgs &a) {
+    return s >= thr || J < a.sink_blocks || J >= I - a.local_blocks + 1;
+}
+
+__global__ void __launch_bounds__(256)
+select_count_kernel(const __grid_constant__ BatchDesc bd, SelectArgs a, const float *__restrict__ score,
+                    int *__restrict__ counts, unsigned char *__restrict__ dense_mask) {
+    const int row = blockIdx.x * 8 + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= bd.total_rows) return;
+    const int r = req_of_row(bd, row);
+    const ReqDesc &rq = bd.req[r];
+    const int local = row - rq.row_base;
+    const int i = local / bd.h_kv, h = local % bd.h_kv;
+    const int I = rq.start / kBlock + i;
+    const long long off = score_row_offset(rq, bd.h_kv, i, h);
+    const float *s = score + off;
+    const float thr = a.alpha * warp_row_max(s, I + 1, lane);
+    int cnt = 0;
+    for (int J = lane; J <= I; J += 32) {
+        bool k = keep_block(__ldg(s + J), thr, J, I, a);
+        cnt += k;
+        if (dense_mask) dense_mask[off + J] = (unsigned char)k;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0) counts[row] = cnt;
+}
+
+// Exclusive scan of counts[0..n) into row_ptr[0..n], nnz = row_ptr[n].
+__global__ void __launch_bounds__(1024)
+scan_kernel(const int *__restrict__ counts, int n, int *__restrict__ row_ptr, int *__restrict__ nnz) {
+    __shared__ int warp_tot[32];
+    const int tid = threadIdx.x;
+    const int per = (n + 1023) / 1024;
+    const int b = tid * per, e = min(n, b + per);
+    int sum = 0;
+    for (int k = b; k < e; ++k) sum += counts[k];
+    // inclusive scan of the per-thread sums
+    int lane = tid % 32, w = tid / 32;
+    int v = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    if (lane == 31) warp_tot[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        int t = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int u = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += u;
+        }
+        warp_tot[lane] = t;
+    }
+    __syncthreads();
+    int run = v - sum + (w > 0 ? warp_tot[w - 1] : 0);
+    for (int k = b; k < e; ++k) {
+        row_ptr[k] = run;
+        run += counts[k];
+    }
+    if (tid == 1023) {
+        int total = warp_tot[31];
+        row_ptr[n] = total;
+        *nnz = total;
+    }
+}
+
+__global__ void __launch_bounds__(256)
+select_compact_kernel(const __grid_constant__ BatchDesc bd, SelectArgs a, const float *__restrict__ score,
+                      const int *__restrict__ row_ptr, int *__restrict__ col_idx,
+                      long long col_capacity, int *status) {
+    const int row = blockIdx.x * 8 + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= bd.total_rows) return;
+    const int r = req_of_row(bd, row);
+    const ReqDesc &rq = bd.req[r];
+    const int local = row - rq.row_base;
+    const int i = local / bd.h_kv, h = local % bd.h_kv;
+    const int I = rq.start / kBlock + i;
+    const float *s = score + score_row_offset(rq, bd.h_kv, i, h);
+    const float thr = a.alpha * warp_row_max(s, I + 1, lane);
+    int pos = row_ptr[row];
+    if ((long long)row_ptr[row + 1] > col_capacity) {
+        if (lane == 0) set_status(status, FP_ERR_INVALID);
+        return;
+    }
+    for (int J0 = 0; J0 <= I; J0 += 32) {
+        int J = J0 + lane;
+        bool k = J <= I && keep_block(__ldg(s + J), thr, J, I, a);
+        unsigned m = __ballot_sync(0xffffffffu, k);
+        if (k) col_idx[pos + __popc(m & ((1u << lane) - 1u))] = J;
+        pos += __popc(m);
+    }
+}
+
+cudaError_t launch_select(const BatchDesc &bd, float alpha, int sink_blocks, int local_blocks,
+                          const float *score, int *counts, int *row_ptr, int *col_idx,
+                          long long col_capacity, int *nnz, unsigned char *dense_mask, int *status,
+                          cudaStream_t st) {
+    SelectArgs a{alpha, sink_blocks, local_blocks};
+    int grid = (bd.total_rows + 7) / 8;
+    select_count_kernel<<<grid, 256, 0, st>>>(bd, a, score, counts, dense_mask);
+    scan_kernel<<<1, 1024, 0, st>>>(counts, bd.total_rows, row_ptr, nnz);
+    select_compact_kernel<<<grid, 256, 0, st>>>(bd, a, score, row_ptr, col_idx, col_capacity, status);
+    return cudaGetLastError();
+}
+
+}  // namespace fp

@@ -1,0 +1,147 @@
+"""CUDA path (through the C ABI) against the float64 oracle, stage by stage:
+pooled means, block scores, keep masks / CSR (bit-exact outside the flagged
+near-threshold band), and the attention output (max-abs 2e-2, mean-abs 2e-3
+for bf16)."""
+import numpy as np
+import pytest
+
+from block_sparse_long_fp_gb300 import synth
+from parity_util import (check_outputs, check_pool, check_scores_and_index, density, gpu_stage_outputs,
+                         oracle_outputs)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_sparse_long_fp_gb300 import build
+    build.build()
+
+
+def full_parity(spec, alpha=0.1, mean_corr=True, rows_per_request=None):
+    import oracle
+    case = synth.make_case(spec)
+    ref = oracle.discover_and_select(case, alpha=alpha)
+    g = gpu_stage_outputs(case, alpha=alpha, mean_corr=mean_corr)
+    assert g["status"] == 0
+    check_pool(case, g, ref)
+    flips = check_scores_and_index(case, g, ref)
+    oref = oracle_outputs(case, ref, mean_corr, rows_per_request=rows_per_request)
+    emax, emean = check_outputs(case, g, oref)
+    return dict(density=density(case, ref), flips=flips, emax=emax, emean=emean)
+
+
+@pytest.mark.parametrize("mean_corr", [True, False])
+def test_tiny_workload(mean_corr):
+    """2K tokens, 4 query heads on 1 kv head, contiguous KV (workload 1)."""
+    full_parity(synth.config_spec(1), mean_corr=mean_corr)
+
+
+@pytest.mark.parametrize("mean_corr", [True, False])
+def test_tiny_workload_sharp_logits_skips_blocks(mean_corr):
+    """Queries scaled by 8: most blocks fall below alpha * max, so the
+    mean-correction tiles and real skipping are exercised."""
+    r = full_parity(synth.config_spec(1, logit_scale=8.0), mean_corr=mean_corr)
+    assert r["density"] < 0.8
+
+
+@pytest.mark.parametrize("page,layout", [(16, "shuffled"), (64, "interleaved"), (128, "shuffled"),
+                                         (256, "contiguous")])
+def test_varlen_chunked_ragged(page, layout):
+    """Several requests in one paged pool: ragged lengths, a one-token
+    request and chunks whose queries start at positions 512 and 128."""
+    spec = synth.Spec("varlen-small", [(300, 0), (1000, 0), (256, 512), (1, 128), (640, 0)], 8, 2,
+                      page_size=page, layout=layout, n_needles=2, logit_scale=6.0, config_id=60 + page)
+    full_parity(spec)
+
+
+def test_random_index_attention_only():
+    """fp_sparse_attn alone on a random CSR (diagonal + each earlier block
+    with probability 0.3), compared with the oracle on the same index."""
+    import math
+    import torch
+    import oracle
+    from block_sparse_long_fp_gb300 import fprefill
+    spec = synth.Spec("rand-csr", [(1536, 0), (700, 256)], 8, 2, page_size=32, layout="shuffled",
+                      n_needles=1, config_id=71)
+    case = synth.make_case(spec)
+    rows = synth.random_keep_lists(case, 0.3, seed=5)
+    row_ptr = np.zeros(len(rows) + 1, np.int32)
+    row_ptr[1:] = np.cumsum([len(x) for x in rows])
+    col_idx = np.concatenate(rows).astype(np.int32)
+    layer = fprefill.layer_from_case(case)
+    k_mean, v_mean, _ = layer.discover()
+    rp = torch.from_numpy(row_ptr).cuda()
+    ci = torch.from_numpy(col_idx).cuda()
+    out, lse = layer.sparse_attn(rp, ci, k_mean, v_mean)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    g = dict(out=out.float().cpu().numpy(), lse=lse.cpu().numpy())
+    k = 0
+    oref = []
+    for r, (lq, start) in enumerate(spec.requests):
+        q = oracle.request_q(case, r)
+        kk, vv = oracle.request_kv(case, r)
+        kbar, vbar = oracle.pool(kk, 128), oracle.pool(vv, 128)
+        nqb = -(-lq // 128)
+        keep = np.zeros((nqb, spec.h_kv, kbar.shape[0]), np.uint8)
+        for i in range(nqb):
+            for h in range(spec.h_kv):
+                keep[i, h, rows[k]] = 1
+                k += 1
+        qi = np.repeat(np.arange(lq), spec.h_q)
+        qh = np.tile(np.arange(spec.h_q), lq)
+        o, l = oracle.attn_rows(q, start, kk, vv, kbar, vbar, 128, 1 / math.sqrt(128), keep, True, qi, qh)
+        oref.append((qi, qh, o, l))
+    check_outputs(case, g, oref)
+
+
+def test_dense_path_equals_causal_softmax():
+    import oracle
+    spec = synth.Spec("dense", [(1000, 0), (384, 256)], 4, 2, page_size=64, layout="shuffled",
+                      n_needles=1, config_id=72)
+    case = synth.make_case(spec)
+    ref = oracle.discover_and_select(case)
+    g = gpu_stage_outputs(case, dense=True)
+    assert g["status"] == 0
+    oref = oracle_outputs(case, ref, mean_corr=False, dense=True)
+    check_outputs(case, g, oref)
+
+
+def test_page_table_entry_out_of_range_sets_status():
+    """A corrupted page-table entry is caught by the kernels' bounds checks:
+    the status word reports it and the run completes."""
+    import torch
+    from block_sparse_long_fp_gb300 import fprefill
+    spec = synth.Spec("bad-page", [(512, 0)], 4, 2, page_size=64, layout="contiguous", config_id=73)
+    case = synth.make_case(spec)
+    case.block_table[0, 3] = case.k_cache.shape[0] + 5
+    layer = fprefill.layer_from_case(case)
+    k_mean, v_mean, score = layer.discover()
+    layer.dense_attn()
+    torch.cuda.synchronize()
+    assert layer.device_status() == fprefill.FP_ERR_DEVICE_BOUNDS
+
+
+@pytest.mark.slow
+def test_llama8b_32k_sampled():
+    """Workload 2 (32K, 32/8 heads, shuffled 64-token pages): every pooled
+    block, a sample of score rows and of output rows."""
+    import oracle
+    spec = synth.config_spec(2)
+    case = synth.make_case(spec)
+    rng = np.random.default_rng(1)
+    sample = lambda r, nqb, hkv: np.unique(np.concatenate([rng.integers(0, nqb * hkv, 24),
+                                                           [0, nqb * hkv - 1]]))
+    ref = oracle.discover_and_select(case, row_subset=sample)
+    g = gpu_stage_outputs(case)
+    assert g["status"] == 0
+    check_pool(case, g, ref)
+    check_scores_and_index_sampled(case, g, ref)
+
+
+def check_scores_and_index_sampled(case, g, ref):
+    check_scores_and_index(case, g, ref)
