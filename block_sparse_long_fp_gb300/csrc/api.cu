@@ -99,7 +99,7 @@ int *status_ptr(void *ws) { return reinterpret_cast<int *>(ws); }
 size_t attn_ws_bytes(const BatchDesc &bd) {
     size_t n = kWsHeaderBytes;
     n += align_up((size_t)bd.total_rows * (bd.g / 2 > 0 ? bd.g / 2 : 1) * sizeof(int), 256);
-    n += 2 * align_up((size_t)bd.total_kb * bd.h_kv * kHeadDim * 2, 256);
+    n += 2 * align_up((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2, 256);
     return n;
 }
 
@@ -233,7 +233,7 @@ static fp_status run_attn(const fp_problem *p, const fp_params *prm, const int *
     L.work = reinterpret_cast<int *>(w + off);
     off += align_up((size_t)bd.total_rows * (bd.g / 2) * sizeof(int), 256);
     L.km16 = reinterpret_cast<__nv_bfloat16 *>(w + off);
-    off += align_up((size_t)bd.total_kb * bd.h_kv * kHeadDim * 2, 256);
+    off += align_up((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2, 256);
     L.vm16 = reinterpret_cast<__nv_bfloat16 *>(w + off);
     L.wait_ns = g_wait_ns;
     return (fp_status)launch_attn(L, (cudaStream_t)stream);

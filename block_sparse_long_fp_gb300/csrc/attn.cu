@@ -17,7 +17,7 @@
 //    means);
 //  * warp 1 issues tcgen05 MMAs: S_t = Q_t K^T into TMEM, then O_t += P_t V
 //    with P_t read from TMEM (it overwrites S_t as packed bf16);
-//  * warps 2-5 / 6-9 are the softmax warpgroups of tile 0 / tile 1: they read
+//  * warps 4-7 / 8-11 are the softmax warpgroups of tile 0 / tile 1: they read
 //    S from TMEM, apply the causal mask or the mean-token bias log2(n_J),
 //    keep the running max (rescaling O in TMEM only when the max grows by
 //    more than 2^8) and write P back to TMEM;
@@ -28,6 +28,9 @@
 //    128-wide tiles of block means that contain at least one skipped block;
 //    the dense path walks J = 0..I with no mean tiles.
 // Every mbarrier wait is bounded (status FP_ERR_TIMEOUT instead of a hang).
+#include <stdio.h>
+#include <stdlib.h>
+
 #include "common.cuh"
 #include "sm100.cuh"
 #include "launch.cuh"
@@ -36,7 +39,13 @@ namespace fp {
 
 using namespace sm100;
 
-constexpr int kAttnThreads = 320;
+constexpr int kAttnThreads = 384;     // 3 warpgroups: control (TMA, MMA), softmax tile 0, tile 1
+// register split (setmaxnreg): the launch grants 168 per thread; the control
+// warpgroup gives some back so the softmax warpgroups can hold a whole
+// 128-column row of S: 96*128 + 2*200*128 <= 168*384.
+constexpr int kRegsControl = 96;
+constexpr int kRegsSoftmax = 200;
+static_assert(kRegsControl * 128 + 2 * kRegsSoftmax * 128 <= 168 * kAttnThreads, "register split");
 constexpr int kTileBytes = kBlock * kHeadDim * 2;          // 32 KB: one 128 x 128 bf16 tile
 constexpr int kHalfBytes = kTileBytes / 2;                 // 64 columns of d
 constexpr int kSmemQ = 0;
@@ -73,7 +82,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtensorMap tmQ,
             const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
             const __grid_constant__ CUtensorMap tmKm, const __grid_constant__ CUtensorMap tmVm,
@@ -160,9 +169,10 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
     // do no work, so a broken launch ends in one wait limit, not one per CTA
     const bool dead = a.status && *reinterpret_cast<volatile int *>(a.status) == FP_ERR_TIMEOUT;
 
-    if (dead) {
-    } else if (n_items > 0) {
-        if (warp == 0) {
+    // each role's code sits under its own register budget
+    if (warp < 4) {
+        setmaxnreg_dec<kRegsControl>();
+        if (!dead && n_items > 0 && warp == 0) {
             // ================= TMA producer =================
             if (lane == 0) {
                 tma_prefetch_desc(&tmQ);
@@ -214,7 +224,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 }
             producer_done:;
             }
-        } else if (warp == 1) {
+        } else if (!dead && n_items > 0 && warp == 1) {
             // ================= MMA issuer =================
             if (lane == 0) {
                 constexpr uint32_t idS = idesc_bf16(128, 128, false);
@@ -274,9 +284,13 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 }
             mma_done:;
             }
-        } else {
+        }
+    } else {
+        setmaxnreg_inc<kRegsSoftmax>();
+        if (dead) {
+        } else if (n_items > 0) {
             // ================= softmax warpgroups =================
-            const int t = (warp - 2) / 4;                 // tile
+            const int t = (warp - 4) / 4;                 // tile
             const int quarter = warp % 4;                 // TMEM lane quarter of this warp
             const int rowt = quarter * 32 + lane;         // row of the tile
             const int qi = il * kBlock + rowt;            // query index inside the request
@@ -347,8 +361,10 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     for (int e = 0; e < 32; ++e) {
                         const float p0 = fast_exp2(x[64 * half + 2 * e] - ms);
                         const float p1 = fast_exp2(x[64 * half + 2 * e + 1] - ms);
-                        rs += p0 + p1;
                         pk[e] = pack_bf16(p0, p1);
+                        // the denominator sums the same bf16-rounded weights the MMA
+                        // multiplies, so the weights of a row sum to exactly one
+                        rs += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
                     }
                     tmem_st32(tS + 32 * half, pk);
                 }
@@ -399,10 +415,9 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     a.lse[(long long)head * bd.total_q + rq.q_off + qi] =
                         l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
             }
-        }
-    } else if (warp >= 2) {
+        } else {
         // a row with no term at all: O = 0, LSE = -inf
-        const int t = (warp - 2) / 4;
+        const int t = (warp - 4) / 4;
         const int rowt = (warp % 4) * 32 + lane;
         const int qi = il * kBlock + rowt;
         if (qi < rq.lq) {
@@ -410,6 +425,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             __nv_bfloat16 *dst = a.out + ((long long)(rq.q_off + qi) * bd.h_q + head) * kHeadDim;
             for (int c = 0; c < kHeadDim; c += 8) *reinterpret_cast<uint4 *>(dst + c) = make_uint4(0, 0, 0, 0);
             if (a.lse) a.lse[(long long)head * bd.total_q + rq.q_off + qi] = -INFINITY;
+        }
         }
     }
 
@@ -458,12 +474,14 @@ sched_kernel(const __grid_constant__ BatchDesc bd, const int *__restrict__ row_p
     }
 }
 
-// fp32 block means -> bf16 operands of the mean tiles
+// fp32 block means -> bf16 operands of the mean tiles; [n, n_pad) is zeroed
 __global__ void to_bf16_kernel(const float *__restrict__ a, const float *__restrict__ b,
-                               __nv_bfloat16 *__restrict__ ao, __nv_bfloat16 *__restrict__ bo, long long n) {
-    for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n; k += (long long)gridDim.x * blockDim.x) {
-        ao[k] = __float2bfloat16_rn(a[k]);
-        bo[k] = __float2bfloat16_rn(b[k]);
+                               __nv_bfloat16 *__restrict__ ao, __nv_bfloat16 *__restrict__ bo, long long n,
+                               long long n_pad) {
+    for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n_pad;
+         k += (long long)gridDim.x * blockDim.x) {
+        ao[k] = __float2bfloat16_rn(k < n ? a[k] : 0.f);
+        bo[k] = __float2bfloat16_rn(k < n ? b[k] : 0.f);
     }
 }
 
@@ -487,10 +505,27 @@ static EncodeTiledFn encode_fn() {
 
 // 3-D bf16 map over [n2][n1][128] with strides (in elements) s1, s2; box
 // (64, 1, box2), 128-byte swizzle, zero fill out of bounds.
+static bool debug_on() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("FPREFILL_DEBUG");
+        v = (e && *e && *e != '0') ? 1 : 0;
+    }
+    return v == 1;
+}
+
+static int fail(const char *what, int code) {
+    if (debug_on()) fprintf(stderr, "[fprefill] %s failed (%d)\n", what, code);
+    return FP_ERR_CUDA;
+}
+
 static bool make_map(CUtensorMap *m, const void *base, long long n1, long long n2, long long s1, long long s2,
                      int box2) {
     EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
+    if (!fn) {
+        fail("cuTensorMapEncodeTiled lookup", 0);
+        return false;
+    }
     cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)n1, (cuuint64_t)n2};
     cuuint64_t strides[2] = {(cuuint64_t)(s1 * 2), (cuuint64_t)(s2 * 2)};
     cuuint32_t box[3] = {64, 1, (cuuint32_t)box2};
@@ -498,6 +533,9 @@ static bool make_map(CUtensorMap *m, const void *base, long long n1, long long n
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS && debug_on())
+        fprintf(stderr, "[fprefill] tensor map dims (128,%lld,%lld) strides (%lld,%lld) box2 %d: CUresult %d\n",
+                n1, n2, s1 * 2, s2 * 2, box2, (int)r);
     return r == CUDA_SUCCESS;
 }
 
@@ -514,22 +552,29 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     CUtensorMap tmQ, tmK, tmV, tmKm, tmVm;
     const long long total_q = bd.total_q;
     const long long tokens = (long long)L.num_pages * L.page_size;
-    if (!make_map(&tmQ, L.q, bd.h_q, total_q, L.q_stride_head, L.q_stride_tok, kBlock)) return FP_ERR_CUDA;
-    if (!make_map(&tmK, L.k_cache, bd.h_kv, tokens, kHeadDim, (long long)bd.h_kv * kHeadDim, rpb)) return FP_ERR_CUDA;
-    if (!make_map(&tmV, L.v_cache, bd.h_kv, tokens, kHeadDim, (long long)bd.h_kv * kHeadDim, rpb)) return FP_ERR_CUDA;
+    if (!make_map(&tmQ, L.q, bd.h_q, total_q, L.q_stride_head, L.q_stride_tok, kBlock)) return fail("Q map", 0);
+    if (!make_map(&tmK, L.k_cache, bd.h_kv, tokens, kHeadDim, (long long)bd.h_kv * kHeadDim, rpb))
+        return fail("K map", 0);
+    if (!make_map(&tmV, L.v_cache, bd.h_kv, tokens, kHeadDim, (long long)bd.h_kv * kHeadDim, rpb))
+        return fail("V map", 0);
     const bool use_means = sparse && L.mean_corr;
+    cudaError_t e;
     if (use_means) {
+        // rows past the last block (padding up to one full 128-row box) are zero
         const long long n = (long long)bd.total_kb * bd.h_kv * kHeadDim;
-        to_bf16_kernel<<<1024, 256, 0, st>>>(L.k_mean, L.v_mean, L.km16, L.vm16, n);
-        if (!make_map(&tmKm, L.km16, bd.h_kv, bd.total_kb, kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock))
-            return FP_ERR_CUDA;
-        if (!make_map(&tmVm, L.vm16, bd.h_kv, bd.total_kb, kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock))
-            return FP_ERR_CUDA;
+        const long long n_pad = (long long)mean_rows(bd) * bd.h_kv * kHeadDim;
+        to_bf16_kernel<<<1024, 256, 0, st>>>(L.k_mean, L.v_mean, L.km16, L.vm16, n, n_pad);
+        if ((e = cudaGetLastError()) != cudaSuccess) return fail("to_bf16 launch", (int)e);
+        if (!make_map(&tmKm, L.km16, bd.h_kv, mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock))
+            return fail("mean K map", 0);
+        if (!make_map(&tmVm, L.vm16, bd.h_kv, mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock))
+            return fail("mean V map", 0);
     } else {
         tmKm = tmK;     // never read
         tmVm = tmV;
     }
     sched_kernel<<<1, 1024, 0, st>>>(bd, L.row_ptr, n_pairs, use_means ? 1 : 0, L.work);
+    if ((e = cudaGetLastError()) != cudaSuccess) return fail("schedule launch", (int)e);
     AttnArgs a;
     a.row_ptr = L.row_ptr;
     a.col_idx = L.col_idx;
@@ -545,10 +590,15 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     a.lse = L.lse;
     a.status = L.status;
     a.wait_ns = L.wait_ns;
-    if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttn) != cudaSuccess)
-        return FP_ERR_CUDA;
+    if ((e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttn)) !=
+        cudaSuccess)
+        return fail("attention smem attribute", (int)e);
     attn_kernel<<<units, kAttnThreads, kSmemAttn, st>>>(bd, tmQ, tmK, tmV, tmKm, tmVm, a);
-    return cudaGetLastError() == cudaSuccess ? FP_OK : FP_ERR_CUDA;
+    if ((e = cudaGetLastError()) != cudaSuccess) {
+        if (debug_on()) fprintf(stderr, "[fprefill] attention launch: %s\n", cudaGetErrorString(e));
+        return fail("attention launch", (int)e);
+    }
+    return FP_OK;
 }
 
 }  // namespace fp

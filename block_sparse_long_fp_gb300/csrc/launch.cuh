@@ -35,5 +35,7 @@ struct AttnLaunch {
     unsigned long long wait_ns;
 };
 int launch_attn(const AttnLaunch &L, cudaStream_t st);
+// rows of the bf16 block-mean copies: at least one full 128-row TMA box
+inline int mean_rows(const BatchDesc &bd) { return bd.total_kb > kBlock ? bd.total_kb : kBlock; }
 int attn_smem_bytes();
 }  // namespace fp

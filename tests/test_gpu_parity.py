@@ -41,11 +41,13 @@ def test_tiny_workload(mean_corr):
 
 
 @pytest.mark.parametrize("mean_corr", [True, False])
-def test_tiny_workload_sharp_logits_skips_blocks(mean_corr):
-    """Queries scaled by 8: most blocks fall below alpha * max, so the
-    mean-correction tiles and real skipping are exercised."""
-    r = full_parity(synth.config_spec(1, logit_scale=8.0), mean_corr=mean_corr)
-    assert r["density"] < 0.8
+def test_sharp_logits_skip_blocks(mean_corr):
+    """8K tokens, queries scaled by 8: about half of the blocks fall below
+    alpha * max, so skipping and the mean-correction tiles are exercised."""
+    spec = synth.Spec("sharp-8k", [(8192, 0)], 4, 1, page_size=64, layout="shuffled", n_needles=2,
+                      logit_scale=8.0, config_id=1)
+    r = full_parity(spec, mean_corr=mean_corr, rows_per_request=3000)
+    assert r["density"] < 0.7
 
 
 @pytest.mark.parametrize("page,layout", [(16, "shuffled"), (64, "interleaved"), (128, "shuffled"),
