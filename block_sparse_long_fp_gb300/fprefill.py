@@ -68,6 +68,8 @@ def lib():
             "fp_sparse_attn": ([P, PP, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                 c_void_p, c_size_t, c_void_p], c_int),
             "fp_dense_attn": ([P, PP, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
+            "fp_sparse_attn_noalloc": ([P, PP, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                        c_void_p, c_void_p], c_int),
             "fp_reset_status": ([c_void_p, c_void_p], c_int),
             "fp_device_status": ([c_void_p, c_void_p, POINTER(c_int)], c_int),
             "fp_status_string": ([c_int], ctypes.c_char_p),
@@ -216,6 +218,15 @@ class Layer:
         _check(lib().fp_sparse_attn(*self._refs(), _ptr(row_ptr), _ptr(col_idx), _ptr(k_mean), _ptr(v_mean),
                                     _ptr(out), _ptr(lse), _ptr(ws), self.ws_bytes, _stream_handle()),
                "fp_sparse_attn")
+        return out, lse
+
+    def sparse_attn_noalloc(self, row_ptr, col_idx, k_mean, v_mean, out, lse=None, status=None):
+        """fp_sparse_attn_noalloc: same result as sparse_attn, with the
+        library's built-in scratch instead of a workspace (nothing is
+        allocated here either: out, lse and status are the caller's)."""
+        _check(lib().fp_sparse_attn_noalloc(*self._refs(), _ptr(row_ptr), _ptr(col_idx), _ptr(k_mean),
+                                            _ptr(v_mean), _ptr(out), _ptr(lse), _ptr(status),
+                                            _stream_handle()), "fp_sparse_attn_noalloc")
         return out, lse
 
     def dense_attn(self, out=None, lse=None, want_lse=True):

@@ -192,6 +192,38 @@ fp_status fp_sparse_attn(const fp_problem *p, const fp_params *prm, const int *r
                          void *out, float *lse_opt, void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * fp_sparse_attn_noalloc -- fp_sparse_attn for callers that cannot allocate
+ * (no counterpart in the pages: an interface addition of this library).
+ *
+ * For callers that have no way to provide a device workspace: a plugin whose
+ * host framework owns all device memory and hands it none, or a serving loop
+ * held to a fixed device-memory budget where allocating mid-request could fail
+ * or stall the device.  The function allocates nothing: its scratch is one
+ * file-scope device array of FP_NOALLOC_SCRATCH_BYTES, reserved on every GPU
+ * that loads the library until the process exits.  The caller still provides
+ * the inputs and the outputs.
+ *
+ *   Arguments and results as fp_sparse_attn, without ws / ws_bytes.
+ *   status_dev_opt (device int32 [1], may be NULL): receives this call's
+ *     device status word (FP_OK or an fp_status code), in stream order after
+ *     the kernels -- the scratch itself is not visible to the caller.
+ *   Returns FP_ERR_WORKSPACE when the problem needs more scratch than
+ *     FP_NOALLOC_SCRATCH_BYTES (compare fp_attn_workspace_size()), before
+ *     touching the GPU; other argument errors as fp_sparse_attn.
+ *   The first call on a device (with that device current) looks up the
+ *     array's device address once and caches it; make that first call before
+ *     any stream capture.
+ *   Every call on a device shares the one array, and the array keeps the last
+ *   call's contents (the call clears what must start at zero).  Calls that
+ *   overlap on the GPU -- on different streams, or from different threads --
+ *   race on it: serialise them.
+ * ------------------------------------------------------------------------- */
+#define FP_NOALLOC_SCRATCH_BYTES (8u << 20)
+fp_status fp_sparse_attn_noalloc(const fp_problem *p, const fp_params *prm, const int *row_ptr,
+                                 const int *col_idx, const float *k_mean, const float *v_mean,
+                                 void *out, float *lse_opt, int *status_dev_opt, void *stream);
+
+/* ---------------------------------------------------------------------------
  * fp_dense_attn -- the same kernel keeping every causal block, no correction
  * (the in-house dense baseline [V2 paper reading 5.3, 5.6]).  Same arguments
  * as fp_sparse_attn without the index and the means.
