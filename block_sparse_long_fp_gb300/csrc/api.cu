@@ -139,9 +139,9 @@ long long fp_total_q(const fp_problem *p) {
 }
 
 size_t fp_discover_workspace_size(const fp_problem *p, const fp_params *prm) {
-    (void)p;
-    (void)prm;
-    return kWsHeaderBytes;
+    BatchDesc bd;
+    if (build_desc(p, prm, &bd) != FP_OK) return 0;
+    return kWsHeaderBytes + (p->dtype == FP_BF16 ? align_up(score_tc_terms_bytes(bd), 256) : 0);
 }
 
 fp_status fp_discover(const fp_problem *p, const fp_params *prm, float *k_mean, float *v_mean, float *score,
@@ -151,18 +151,26 @@ fp_status fp_discover(const fp_problem *p, const fp_params *prm, float *k_mean, 
     if (s != FP_OK) return s;
     if ((s = check_kv(p, bd)) != FP_OK || (s = check_q(p)) != FP_OK) return s;
     if (!k_mean || !v_mean || !score || !aligned16(k_mean) || !aligned16(v_mean)) return FP_ERR_INVALID;
-    if (!ws || ws_bytes < kWsHeaderBytes) return FP_ERR_WORKSPACE;
-    if (score_smem_bytes(bd.max_nkb) > 227 * 1024) return FP_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < fp_discover_workspace_size(p, prm)) return FP_ERR_WORKSPACE;
+    if (p->dtype == FP_E4M3 && score_smem_bytes(bd.max_nkb) > 227 * 1024) return FP_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     const bool fp8 = p->dtype == FP_E4M3;
     if (bd.total_kb > 0 &&
         launch_pool(bd, fp8, p->k_cache, p->v_cache, p->page_size, p->num_pages, p->block_table,
                     p->max_pages_per_seq, p->k_scale, p->v_scale, k_mean, v_mean, status_ptr(ws), st) != cudaSuccess)
         return FP_ERR_CUDA;
-    if (bd.total_rows > 0 &&
-        launch_score(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean, softmax_scale_of(prm, p->d),
-                     score, st) != cudaSuccess)
-        return FP_ERR_CUDA;
+    if (bd.total_rows > 0) {
+        cudaError_t e;
+        if (fp8)
+            e = launch_score(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean,
+                             softmax_scale_of(prm, p->d), score, st);
+        else
+            e = launch_score_tc(bd, p->q, p->q_stride_tok, p->q_stride_head, k_mean, softmax_scale_of(prm, p->d),
+                                score,
+                                reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + kWsHeaderBytes),
+                                status_ptr(ws), g_wait_ns, st);
+        if (e != cudaSuccess) return FP_ERR_CUDA;
+    }
     return FP_OK;
 }
 

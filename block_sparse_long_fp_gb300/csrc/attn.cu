@@ -310,11 +310,14 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) reg_fence(v[c]);
+                // raw logits; masked entries -inf.  The scale and the mean-token
+                // bias are applied inside the exponent: p = 2^(s*c + bias - m).
                 float x[128];
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]) * a.scale_log2;
+                    for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]);
+                float bias = 0.f;
                 if (j < n_kept) {
                     const int J = sparse ? __ldg(a.col_idx + rp0 + j) : j;
                     const int k0 = J * kBlock;
@@ -337,11 +340,18 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     }
 #pragma unroll
                     for (int e = 0; e < 128; ++e)
-                        x[e] = ((w[e >> 5] >> (e & 31)) & 1u) ? x[e] + 7.f : -INFINITY;
+                        if (!((w[e >> 5] >> (e & 31)) & 1u)) x[e] = -INFINITY;
+                    bias = 7.f;
                 }
-                float mx = x[0];
+                // row max: eight independent chains, then a tree
+                float mx8[8];
 #pragma unroll
-                for (int e = 1; e < 128; ++e) mx = fmaxf(mx, x[e]);
+                for (int k = 0; k < 8; ++k) mx8[k] = x[k];
+#pragma unroll
+                for (int e = 8; e < 128; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], x[e]);
+                const float mxr = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                const float mx = mxr * a.scale_log2 + bias;         // log2 units; -inf stays -inf
                 // grow the running max only when it rises by more than 2^8 (rarely);
                 // O is rescaled after P is written (x is dead by then), and the
                 // TMEM round trip runs warp-wide
@@ -352,22 +362,23 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     l *= f;
                     m = mx;
                 }
-                const float ms = m == -INFINITY ? 0.f : m;
-                float rs = 0.f;
+                const float off = bias - (m == -INFINITY ? 0.f : m);
+                float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float p0 = fast_exp2(x[64 * half + 2 * e] - ms);
-                        const float p1 = fast_exp2(x[64 * half + 2 * e + 1] - ms);
+                        const float p0 = fast_exp2(fmaf(x[64 * half + 2 * e], a.scale_log2, off));
+                        const float p1 = fast_exp2(fmaf(x[64 * half + 2 * e + 1], a.scale_log2, off));
                         pk[e] = pack_bf16(p0, p1);
                         // the denominator sums the same bf16-rounded weights the MMA
                         // multiplies, so the weights of a row sum to exactly one
-                        rs += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
+                        rs4[e & 3] += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
                     }
                     tmem_st32(tS + 32 * half, pk);
                 }
+                const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
                 l += rs;
                 if (any_grow && j > 0) {
 #pragma unroll 1

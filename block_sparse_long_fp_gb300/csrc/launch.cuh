@@ -14,6 +14,15 @@ cudaError_t launch_select(const BatchDesc &bd, float alpha, int sink_blocks, int
                           int *counts, int *row_ptr, int *col_idx, long long col_capacity, int *nnz,
                           unsigned char *dense_mask, int *status, cudaStream_t st);
 size_t score_smem_bytes(int max_nkb);
+// tensor-core score map (bf16 inputs): the three bf16 terms of the means live in
+// a workspace of score_tc_terms_bytes()
+int score_tc_rows_pad(const BatchDesc &bd);
+inline size_t score_tc_terms_bytes(const BatchDesc &bd) {
+    return (size_t)3 * score_tc_rows_pad(bd) * bd.h_kv * kHeadDim * 2;
+}
+cudaError_t launch_score_tc(const BatchDesc &bd, const void *q, long long q_stride_tok, long long q_stride_head,
+                            const float *k_mean, float softmax_scale, float *score, __nv_bfloat16 *terms,
+                            int *status, unsigned long long wait_ns, cudaStream_t st);
 
 struct AttnLaunch {
     const BatchDesc *bd;

@@ -147,3 +147,24 @@ def test_llama8b_32k_sampled():
 
 def check_scores_and_index_sampled(case, g, ref):
     check_scores_and_index(case, g, ref)
+
+
+def test_fp8_discover_and_select():
+    """e4m3 inputs with per-head scales: block means of the dequantised
+    values, fp32 scores and the index against the oracle on the same codes."""
+    import oracle
+    spec = synth.Spec("fp8-disc", [(2048, 0), (700, 256)], 8, 2, page_size=64, layout="shuffled",
+                      dtype="e4m3", n_needles=2, logit_scale=6.0, config_id=74)
+    case = synth.make_case(spec)
+    ref = oracle.discover_and_select(case)
+    from block_sparse_long_fp_gb300 import fprefill
+    import torch
+    layer = fprefill.layer_from_case(case)
+    k_mean, v_mean, score = layer.discover()
+    row_ptr, col_idx, nnz = layer.select(score)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    g = dict(k_mean=k_mean.cpu().numpy(), v_mean=v_mean.cpu().numpy(), score=score.cpu().numpy(),
+             row_ptr=row_ptr.cpu().numpy(), col_idx=col_idx.cpu().numpy())
+    check_pool(case, g, ref)
+    check_scores_and_index(case, g, ref)
