@@ -158,6 +158,52 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def measure_layer(layer, spec, steps, warmup, dense_steps, stream, fp8=False):
+    """Time the whole step and each stage on one uploaded layer."""
+    import torch
+    flop = dense_equiv_flop(spec)
+    for _ in range(warmup):
+        _, _, (row_ptr, _, _) = layer.prefill()
+    torch.cuda.synchronize()
+    status = layer.device_status()
+    stats = index_stats(spec, row_ptr.cpu().numpy())
+    ms = cuda_time(lambda: layer.prefill(), steps, stream)
+    k_mean, v_mean, score = layer.discover()
+    rp, ci, nz = layer.select(score)
+    reps = max(2, min(steps, 5))
+    out_buf = torch.empty((layer.total_q, layer.h_q, 128), dtype=torch.bfloat16, device=layer.q.device)
+    ms_disc = cuda_time(lambda: layer.discover(k_mean, v_mean, score), reps, stream)
+    ms_sel = cuda_time(lambda: layer.select(score, rp, ci, nz), reps, stream)
+    ms_attn = cuda_time(lambda: layer.sparse_attn(rp, ci, k_mean, v_mean, out=out_buf, want_lse=False), reps,
+                        stream)
+    ms_dense = None
+    if dense_steps > 0:
+        layer.dense_attn(out=out_buf, want_lse=False)
+        ms_dense = cuda_time(lambda: layer.dense_attn(out=out_buf, want_lse=False), dense_steps, stream)
+    peaks, peak_kind = load_peaks()
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * (2.0 if fp8 else 1.0)
+    attn_flop = stats["kept_flop"] + stats["corr_flop"]
+    achieved = attn_flop / (ms_attn * 1e-3) / 1e12
+    return dict(ms=ms, flop=flop, status=status, stats=stats, ms_disc=ms_disc, ms_sel=ms_sel, ms_attn=ms_attn,
+                ms_dense=ms_dense, achieved=achieved, peak=peak, peak_kind=peak_kind)
+
+
+def summary(m, spec, logit_scale, dtype):
+    return {
+        "dtype": dtype, "logit_scale": logit_scale,
+        "ms_per_layer": round(m["ms"], 4),
+        "dense_equiv_tflops": round(m["flop"] / (m["ms"] * 1e-3) / 1e12, 2),
+        "stages_ms": {"discover": round(m["ms_disc"], 4), "select": round(m["ms_sel"], 4),
+                      "sparse_attn": round(m["ms_attn"], 4)},
+        "density": round(m["stats"]["density"], 5),
+        "attn_tflops": round(m["achieved"], 2), "attn_peak_tflops": m["peak"],
+        "attn_frac": round(m["achieved"] / m["peak"], 4),
+        "dense_attn_ms": None if m["ms_dense"] is None else round(m["ms_dense"], 4),
+        "speedup_vs_own_dense": None if m["ms_dense"] is None else round(m["ms_dense"] / m["ms"], 3),
+        "device_status": m["status"],
+    }
+
+
 def run_ours(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -196,30 +242,42 @@ def run_ours(args, rank, world):
         ms = float(t.item())
     clocks = clk.summary()
 
-    # --- per-stage breakdown and the attention kernel alone ---
-    k_mean, v_mean, score = layer.discover()
-    rp, ci, nz = layer.select(score)
-    reps = max(2, min(args.steps, 5))
-    ms_disc = cuda_time(lambda: layer.discover(k_mean, v_mean, score), reps, stream)
-    ms_sel = cuda_time(lambda: layer.select(score, rp, ci, nz), reps, stream)
-    out_buf = torch.empty_like(layer.q, dtype=torch.bfloat16)
-    ms_attn = cuda_time(lambda: layer.sparse_attn(rp, ci, k_mean, v_mean, out=out_buf, want_lse=False),
-                        reps, stream)
-    ms_dense = None
-    if args.dense_steps > 0:
-        layer.dense_attn(out=out_buf, want_lse=False)
-        ms_dense = cuda_time(lambda: layer.dense_attn(out=out_buf, want_lse=False), args.dense_steps, stream)
+    # --- per-stage breakdown, the attention kernel alone, the dense path ---
+    m = measure_layer(layer, spec, min(args.steps, 5), 1, args.dense_steps, stream)
+    ms_disc, ms_sel, ms_attn, ms_dense = m["ms_disc"], m["ms_sel"], m["ms_attn"], m["ms_dense"]
 
     # --- end to end through the C ABI with host buffers ---
     e2e = None
     if args.e2e_steps > 0:
         e2e = run_e2e(layer, args.e2e_steps, flop)
 
+    # --- variants in the same line: the sparse regime and FP8-e4m3 ---
+    variants = {}
+    if args.variants and rank == 0:
+        if args.logit_scale == 1.0:
+            layer.q.mul_(16.0)                  # exact: a power of two
+            variants["bf16_logit_scale_16"] = summary(
+                measure_layer(layer, spec, min(args.steps, 5), 2, args.dense_steps, stream), spec, 16.0, "bf16")
+            layer.q.div_(16.0)
+        del layer
+        torch.cuda.empty_cache()
+        spec8 = synth.config_spec(args.workload, dtype="e4m3")
+        case8 = synth.make_case(spec8)
+        layer8 = fprefill.layer_from_case(case8, device=dev)
+        variants["e4m3"] = summary(measure_layer(layer8, spec8, min(args.steps, 5), 2, args.dense_steps, stream,
+                                                 fp8=True), spec8, 1.0, "e4m3")
+        layer8.q_scale.mul_(16.0)               # the same sharper logits, exactly, through the scales
+        variants["e4m3_logit_scale_16"] = summary(
+            measure_layer(layer8, spec8, min(args.steps, 5), 2, args.dense_steps, stream, fp8=True), spec8, 16.0,
+            "e4m3")
+        del layer8, case8
+
     peaks, peak_kind = load_peaks()
     attn_flop = stats["kept_flop"] + stats["corr_flop"]
     achieved = attn_flop / (ms_attn * 1e-3) / 1e12
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     value = world * flop / (ms * 1e-3) / 1e12
+    q_bytes = spec.total_q * spec.h_q * spec.d * 2
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -230,7 +288,7 @@ def run_ours(args, rank, world):
                    "page_layout": spec.layout, "alpha": 0.1, "sink_tokens": 256, "local_tokens": 512,
                    "block": 128, "mean_correction": True, "logit_scale": args.logit_scale,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (Q alone is 1 GiB)"},
+                   "l2": f"inputs larger than L2 (Q alone is {q_bytes / 2**20:.0f} MiB)"},
         "ms_per_layer": round(ms, 4),
         "stages_ms": {"discover": round(ms_disc, 4), "select": round(ms_sel, 4),
                       "sparse_attn": round(ms_attn, 4)},
@@ -241,11 +299,13 @@ def run_ours(args, rank, world):
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "kernel": "attn_kernel (fp_sparse_attn)",
                      "peak_source": f"{peak_kind} bf16 sustained (MEASURED_PEAKS.json)"},
-        "gpu_launches": 8 * args.steps,
+        "gpu_launches": 9 * args.steps,
         "device_status": status,
         "clocks": clocks,
         "gen_seconds": round(gen_s, 1),
     }
+    if variants:
+        res["variants"] = variants
     if e2e:
         res["e2e"] = e2e
     return res, case
@@ -367,6 +427,8 @@ def main():
     ap.add_argument("--dense-steps", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-variants", dest="variants", action="store_false",
+                    help="skip the sparse-regime and FP8 variants")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

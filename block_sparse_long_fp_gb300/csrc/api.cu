@@ -96,6 +96,13 @@ float softmax_scale_of(const fp_params *prm, int d) {
 
 int *status_ptr(void *ws) { return reinterpret_cast<int *>(ws); }
 
+// bf16 scores run on the tensor cores while their per-warp column sums fit in
+// shared memory (rows up to 4096 key blocks); e4m3 and longer rows use the
+// fp32 CUDA-core kernel.
+bool use_score_tc(const fp_problem *p, const BatchDesc &bd) {
+    return p->dtype == FP_BF16 && score_tc_smem_bytes(bd.max_nkb) <= 227 * 1024;
+}
+
 size_t attn_ws_bytes(const BatchDesc &bd) {
     size_t n = kWsHeaderBytes;
     n += align_up((size_t)bd.total_rows * (bd.g / 2 > 0 ? bd.g / 2 : 1) * sizeof(int), 256);
@@ -141,7 +148,7 @@ long long fp_total_q(const fp_problem *p) {
 size_t fp_discover_workspace_size(const fp_problem *p, const fp_params *prm) {
     BatchDesc bd;
     if (build_desc(p, prm, &bd) != FP_OK) return 0;
-    return kWsHeaderBytes + (p->dtype == FP_BF16 ? align_up(score_tc_terms_bytes(bd), 256) : 0);
+    return kWsHeaderBytes + (use_score_tc(p, bd) ? align_up(score_tc_terms_bytes(bd), 256) : 0);
 }
 
 fp_status fp_discover(const fp_problem *p, const fp_params *prm, float *k_mean, float *v_mean, float *score,
@@ -152,7 +159,8 @@ fp_status fp_discover(const fp_problem *p, const fp_params *prm, float *k_mean, 
     if ((s = check_kv(p, bd)) != FP_OK || (s = check_q(p)) != FP_OK) return s;
     if (!k_mean || !v_mean || !score || !aligned16(k_mean) || !aligned16(v_mean)) return FP_ERR_INVALID;
     if (!ws || ws_bytes < fp_discover_workspace_size(p, prm)) return FP_ERR_WORKSPACE;
-    if (p->dtype == FP_E4M3 && score_smem_bytes(bd.max_nkb) > 227 * 1024) return FP_ERR_UNSUPPORTED;
+    const bool tc = use_score_tc(p, bd);
+    if (!tc && score_smem_bytes(bd.max_nkb) > 227 * 1024) return FP_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     const bool fp8 = p->dtype == FP_E4M3;
     if (bd.total_kb > 0 &&
@@ -161,7 +169,7 @@ fp_status fp_discover(const fp_problem *p, const fp_params *prm, float *k_mean, 
         return FP_ERR_CUDA;
     if (bd.total_rows > 0) {
         cudaError_t e;
-        if (fp8)
+        if (!tc)
             e = launch_score(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean,
                              softmax_scale_of(prm, p->d), score, st);
         else
@@ -211,7 +219,6 @@ static fp_status run_attn(const fp_problem *p, const fp_params *prm, const int *
     fp_status s = build_desc(p, prm, &bd);
     if (s != FP_OK) return s;
     if ((s = check_kv(p, bd)) != FP_OK || (s = check_q(p)) != FP_OK) return s;
-    if (p->dtype != FP_BF16) return FP_ERR_UNSUPPORTED;
     if (bd.g % 2) return FP_ERR_UNSUPPORTED;
     if (!out || !aligned16(out)) return FP_ERR_INVALID;
     if (!ws || ws_bytes < attn_ws_bytes(bd)) return FP_ERR_WORKSPACE;
@@ -244,6 +251,10 @@ static fp_status run_attn(const fp_problem *p, const fp_params *prm, const int *
     off += align_up((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2, 256);
     L.vm16 = reinterpret_cast<__nv_bfloat16 *>(w + off);
     L.wait_ns = g_wait_ns;
+    L.fp8 = p->dtype == FP_E4M3;
+    L.q_scale = p->q_scale;
+    L.k_scale = p->k_scale;
+    L.v_scale = p->v_scale;
     return (fp_status)launch_attn(L, (cudaStream_t)stream);
 }
 

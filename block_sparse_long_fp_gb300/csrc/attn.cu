@@ -42,9 +42,9 @@ using namespace sm100;
 constexpr int kAttnThreads = 384;     // 3 warpgroups: control (TMA, MMA), softmax tile 0, tile 1
 // register split (setmaxnreg): the launch grants 168 per thread; the control
 // warpgroup gives some back so the softmax warpgroups can hold a whole
-// 128-column row of S: 96*128 + 2*200*128 <= 168*384.
-constexpr int kRegsControl = 96;
-constexpr int kRegsSoftmax = 200;
+// 128-column row of S: 104*128 + 2*192*128 <= 168*384.
+constexpr int kRegsControl = 104;
+constexpr int kRegsSoftmax = 192;
 static_assert(kRegsControl * 128 + 2 * kRegsSoftmax * 128 <= 168 * kAttnThreads, "register split");
 constexpr int kTileBytes = kBlock * kHeadDim * 2;          // 32 KB: one 128 x 128 bf16 tile
 constexpr int kHalfBytes = kTileBytes / 2;                 // 64 columns of d
@@ -70,6 +70,9 @@ struct AttnArgs {
     int n_pairs;              // query-head pairs per kv head
     int mean_corr;
     float scale_log2;         // softmax scale * log2(e)
+    const float *q_scale;     // e4m3 only: per query head / kv head scales
+    const float *k_scale;
+    const float *v_scale;
     __nv_bfloat16 *out;
     float *lse;
     int *status;
@@ -82,6 +85,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// kFp8: q, k, v (and the block-mean tiles) are e4m3 codes with per-head
+// scales; both MMAs run as kind::f8f6f4 and P is stored in TMEM as e4m3 of
+// 256 * p (the scaling of the V2 paper reading, section 4.2 (4), which keeps
+// the weights in e4m3's normal range; it cancels in the ratio).
+template <bool kFp8>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtensorMap tmQ,
             const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -99,6 +107,10 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t sbase = smem_u32(smem);
     auto bar = [&](int k) { return smem_u32(&bars[k]); };
+    // a 128 x 128 tile is 32 KB of bf16 in two 64-column boxes, or 16 KB of
+    // e4m3 in one 128-column box; smem slots are 32 KB either way
+    constexpr int kT = kFp8 ? kTileBytes / 2 : kTileBytes;
+    constexpr int kNH = kFp8 ? 1 : 2;
 
     // ---- the unit ------------------------------------------------------------
     const int unit = a.work[blockIdx.x];
@@ -179,9 +191,9 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 tma_prefetch_desc(&tmK);
                 tma_prefetch_desc(&tmV);
                 const int q_row0 = rq.q_off + il * kBlock;
-                mbar_expect_tx(bar(BAR_Q), 2 * kTileBytes);
+                mbar_expect_tx(bar(BAR_Q), 2 * kT);
                 for (int t = 0; t < 2; ++t)
-                    for (int hf = 0; hf < 2; ++hf)
+                    for (int hf = 0; hf < kNH; ++hf)
                         tma_load_3d(sbase + kSmemQ + t * kTileBytes + hf * kHalfBytes, &tmQ, bar(BAR_Q),
                                     hf * 64, hq0 + t, q_row0);
                 const int rpb = a.page_size < kBlock ? a.page_size : kBlock;   // rows per box
@@ -200,7 +212,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                                                  a.status, a.wait_ns))
                             goto producer_done;
                         const uint32_t dst = sbase + (op == 0 ? kSmemK : kSmemV) + s * kTileBytes;
-                        mbar_expect_tx(full, kTileBytes);
+                        mbar_expect_tx(full, kT);
                         if (kept) {
                             const CUtensorMap *tm = op == 0 ? &tmK : &tmV;
                             for (int sub = 0; sub < kBlock / rpb; ++sub) {
@@ -212,12 +224,12 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                                     if (pg >= 0 && pg < a.num_pages) z = pg * a.page_size + tok % a.page_size;
                                     else set_status(a.status, FP_ERR_DEVICE_BOUNDS);
                                 }
-                                for (int hf = 0; hf < 2; ++hf)
+                                for (int hf = 0; hf < kNH; ++hf)
                                     tma_load_3d(dst + hf * kHalfBytes + sub * rpb * 128, tm, full, hf * 64, h, z);
                             }
                         } else {
                             const CUtensorMap *tm = op == 0 ? &tmKm : &tmVm;
-                            for (int hf = 0; hf < 2; ++hf)
+                            for (int hf = 0; hf < kNH; ++hf)
                                 tma_load_3d(dst + hf * kHalfBytes, tm, full, hf * 64, h, rq.kb_base + c * kBlock);
                         }
                     }
@@ -227,24 +239,32 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
         } else if (!dead && n_items > 0 && warp == 1) {
             // ================= MMA issuer =================
             if (lane == 0) {
-                constexpr uint32_t idS = idesc_bf16(128, 128, false);
-                constexpr uint32_t idPV = idesc_bf16(128, 128, true);
+                constexpr uint32_t idS = kFp8 ? idesc_e4m3(128, 128, false) : idesc_bf16(128, 128, false);
+                constexpr uint32_t idPV = kFp8 ? idesc_e4m3(128, 128, true) : idesc_bf16(128, 128, true);
+                constexpr int kKSteps = kFp8 ? 4 : 8;                // K = 32 (e4m3) or 16 (bf16) per MMA
+                constexpr int kKeysPerStep = kFp8 ? 32 : 16;
+                // descriptors differ only in the start address: add offsets (in 16-byte units)
+                const uint64_t qdesc = smem_desc_sw128(sbase + kSmemQ, 16, 1024);
+                const uint64_t kdesc = smem_desc_sw128(sbase + kSmemK, 16, 1024);
+                const uint64_t vdesc = smem_desc_sw128(sbase + kSmemV, kFp8 ? 16 : kHalfBytes, 1024);
                 auto issue_S = [&](int t, int s) {
-                    const uint32_t qa = sbase + kSmemQ + t * kTileBytes;
-                    const uint32_t kb = sbase + kSmemK + s * kTileBytes;
+                    const uint64_t qd = qdesc + ((t * kTileBytes) >> 4);
+                    const uint64_t kd = kdesc + ((s * kTileBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        mma_ss(tmem + t * 256, smem_desc_sw128(qa + off, 16, 1024),
-                               smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0);
+                    for (int kk = 0; kk < kKSteps; ++kk) {
+                        const uint32_t off = (kFp8 ? kk * 32 : (kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                        if constexpr (kFp8) mma_ss_f8(tmem + t * 256, qd + off, kd + off, idS, kk > 0);
+                        else mma_ss(tmem + t * 256, qd + off, kd + off, idS, kk > 0);
                     }
                 };
                 auto issue_PV = [&](int t, int s, bool acc) {
-                    const uint32_t vb = sbase + kSmemV + s * kTileBytes;
+                    const uint64_t vd = vdesc + ((s * kTileBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kBlock / 16; ++kk)
-                        mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8,
-                               smem_desc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024), idPV, (acc || kk > 0));
+                    for (int kk = 0; kk < kKSteps; ++kk) {
+                        const uint64_t b = vd + ((kk * kKeysPerStep * 128) >> 4);
+                        if constexpr (kFp8) mma_ts_f8(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, b, idPV, (acc || kk > 0));
+                        else mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, b, idPV, (acc || kk > 0));
+                    }
                 };
                 if (!mbar_wait(bar(BAR_Q), 0, abort_flag, a.status, a.wait_ns)) goto mma_done;
                 if (!mbar_wait(bar(BAR_KF), 0, abort_flag, a.status, a.wait_ns)) goto mma_done;
@@ -300,6 +320,13 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             const uint32_t tO = tS + 128;
             float m = -INFINITY, l = 0.f;
             bool ok = true;
+            // logit scale (log2 units): e4m3 codes carry the per-head scales
+            const float csc = kFp8 ? a.scale_log2 * __ldg(a.q_scale + hq0 + t) * __ldg(a.k_scale + h) : a.scale_log2;
+            // the running max moves only when it grows by more than kTau (bf16
+            // tolerates weights up to 2^8).  For e4m3 it always follows the max, so
+            // the largest weight of a row is exactly 256 = e4m3(256 * 1) and only
+            // the smaller weights carry e4m3 rounding.
+            constexpr float kTau = kFp8 ? 0.f : 8.f;
             for (int j = 0; j < n_items && ok; ++j) {
                 const bool got = mbar_wait(bar(BAR_SF + t), j & 1, abort_flag, a.status, a.wait_ns);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }   // tcgen05.ld needs the whole warp
@@ -343,19 +370,18 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         if (!((w[e >> 5] >> (e & 31)) & 1u)) x[e] = -INFINITY;
                     bias = 7.f;
                 }
-                // row max: eight independent chains, then a tree
+                // row max: eight independent chains of three-input max, then a tree
                 float mx8[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) mx8[k] = x[k];
 #pragma unroll
-                for (int e = 8; e < 128; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], x[e]);
-                const float mxr = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-                const float mx = mxr * a.scale_log2 + bias;         // log2 units; -inf stays -inf
+                for (int e = 8; e < 128; e += 2) mx8[(e >> 1) & 7] = max3f(mx8[(e >> 1) & 7], x[e], x[e + 1]);
+                const float mxr = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+                const float mx = mxr * csc + bias;                   // log2 units; -inf stays -inf
                 // grow the running max only when it rises by more than 2^8 (rarely);
                 // O is rescaled after P is written (x is dead by then), and the
                 // TMEM round trip runs warp-wide
-                const bool grow = mx > m + 8.f;
+                const bool grow = mx > m + kTau;
                 const bool any_grow = __any_sync(0xffffffffu, grow);
                 const float f = grow ? fast_exp2(m - mx) : 1.f;   // 0 when m = -inf
                 if (grow) {
@@ -363,22 +389,57 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     m = mx;
                 }
                 const float off = bias - (m == -INFINITY ? 0.f : m);
-                float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+                float rs;
+                // exponents as paired FMAs: (s0, s1) * c + off
+                const uint64_t cc = f2_pack(csc, csc);
+                if constexpr (!kFp8) {
+                    const uint64_t oo = f2_pack(off, off);
+                    uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            float z0, z1;
+                            f2_unpack(f2_fma(f2_pack(x[64 * half + 2 * e], x[64 * half + 2 * e + 1]), cc, oo), z0, z1);
+                            pk[e] = pack_bf16(fast_exp2(z0), fast_exp2(z1));
+                            // the denominator sums the same bf16-rounded weights the MMA
+                            // multiplies, so the weights of a row sum to exactly one
+                            acc2[e & 1] = f2_add(acc2[e & 1], f2_pack(__uint_as_float(pk[e] << 16),
+                                                                      __uint_as_float(pk[e] & 0xffff0000u)));
+                        }
+                        tmem_st32(tS + 32 * half, pk);
+                    }
+                    float r0, r1, r2, r3;
+                    f2_unpack(acc2[0], r0, r1);
+                    f2_unpack(acc2[1], r2, r3);
+                    rs = (r0 + r1) + (r2 + r3);
+                } else {
+                    // e4m3 of 256 * p: four weights per TMEM column; the denominator
+                    // sums the decoded weights (in half2, <= 128 * 256 < 65504)
+                    const uint64_t oo = f2_pack(off + 8.f, off + 8.f);
                     uint32_t pk[32];
+                    __half2 hs[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) hs[k] = __float2half2_rn(0.f);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float p0 = fast_exp2(fmaf(x[64 * half + 2 * e], a.scale_log2, off));
-                        const float p1 = fast_exp2(fmaf(x[64 * half + 2 * e + 1], a.scale_log2, off));
-                        pk[e] = pack_bf16(p0, p1);
-                        // the denominator sums the same bf16-rounded weights the MMA
-                        // multiplies, so the weights of a row sum to exactly one
-                        rs4[e & 3] += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
+                        float z0, z1, z2, z3;
+                        f2_unpack(f2_fma(f2_pack(x[4 * e], x[4 * e + 1]), cc, oo), z0, z1);
+                        f2_unpack(f2_fma(f2_pack(x[4 * e + 2], x[4 * e + 3]), cc, oo), z2, z3);
+                        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                            make_float2(fast_exp2(z0), fast_exp2(z1)), __NV_SATFINITE, __NV_E4M3);
+                        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                            make_float2(fast_exp2(z2), fast_exp2(z3)), __NV_SATFINITE, __NV_E4M3);
+                        pk[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+                        hs[e & 3] = __hadd2(hs[e & 3], __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3)),
+                                                               __half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3))));
                     }
-                    tmem_st32(tS + 32 * half, pk);
+                    tmem_st32(tS, pk);
+                    const float2 f0 = __half22float2(hs[0]), f1 = __half22float2(hs[1]);
+                    const float2 f2 = __half22float2(hs[2]), f3 = __half22float2(hs[3]);
+                    rs = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
                 }
-                const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
                 l += rs;
                 if (any_grow && j > 0) {
 #pragma unroll 1
@@ -402,7 +463,9 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             const bool fin = ok && mbar_wait(bar(BAR_OF + t), 0, abort_flag, a.status, a.wait_ns);
             if (__all_sync(0xffffffffu, fin)) {
                 tc_fence_after();
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+                // O = (sum of weights * v codes) * v_scale / (sum of weights); for e4m3
+                // both sums carry the factor 256, which cancels
+                const float inv = l > 0.f ? (kFp8 ? __ldg(a.v_scale + h) : 1.f) / l : 0.f;
                 __nv_bfloat16 *dst = a.out + ((long long)(rq.q_off + qi) * bd.h_q + head) * kHeadDim;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -424,7 +487,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 }
                 if (valid && a.lse)
                     a.lse[(long long)head * bd.total_q + rq.q_off + qi] =
-                        l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+                        l > 0.f ? (m + __log2f(l) - (kFp8 ? 8.f : 0.f)) * 0.6931471805599453f : -INFINITY;
             }
         } else {
         // a row with no term at all: O = 0, LSE = -inf
@@ -497,6 +560,22 @@ __global__ void to_bf16_kernel(const float *__restrict__ a, const float *__restr
 }
 
 
+// fp32 block means -> e4m3 codes with the per-head K / V scales (block means
+// never exceed the largest |value| the scale maps to 448); [n, n_pad) is zeroed
+__global__ void to_e4m3_kernel(const float *__restrict__ a, const float *__restrict__ b, const float *__restrict__ sa,
+                               const float *__restrict__ sb, uint8_t *__restrict__ ao, uint8_t *__restrict__ bo,
+                               long long n, long long n_pad, int h_kv) {
+    for (long long k = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 2; k < n_pad;
+         k += (long long)gridDim.x * blockDim.x * 2) {
+        const int h = (int)((k / kHeadDim) % h_kv);
+        const float ia = 1.f / __ldg(sa + h), ib = 1.f / __ldg(sb + h);
+        const float2 va = k < n ? make_float2(a[k] * ia, a[k + 1] * ia) : make_float2(0.f, 0.f);
+        const float2 vb = k < n ? make_float2(b[k] * ib, b[k + 1] * ib) : make_float2(0.f, 0.f);
+        *reinterpret_cast<__nv_fp8x2_storage_t *>(ao + k) = __nv_cvt_float2_to_fp8x2(va, __NV_SATFINITE, __NV_E4M3);
+        *reinterpret_cast<__nv_fp8x2_storage_t *>(bo + k) = __nv_cvt_float2_to_fp8x2(vb, __NV_SATFINITE, __NV_E4M3);
+    }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -514,8 +593,6 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 3-D bf16 map over [n2][n1][128] with strides (in elements) s1, s2; box
-// (64, 1, box2), 128-byte swizzle, zero fill out of bounds.
 static bool debug_on() {
     static int v = -1;
     if (v < 0) {
@@ -530,23 +607,27 @@ static int fail(const char *what, int code) {
     return FP_ERR_CUDA;
 }
 
+// 3-D map over [n2][n1][128] elements (bf16, or bytes for e4m3) with strides
+// (in elements) s1, s2; box (one 128-byte row of d, 1, box2), 128-byte
+// swizzle, zero fill out of bounds.
 static bool make_map(CUtensorMap *m, const void *base, long long n1, long long n2, long long s1, long long s2,
-                     int box2) {
+                     int box2, bool fp8 = false) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) {
         fail("cuTensorMapEncodeTiled lookup", 0);
         return false;
     }
+    const int esz = fp8 ? 1 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)n1, (cuuint64_t)n2};
-    cuuint64_t strides[2] = {(cuuint64_t)(s1 * 2), (cuuint64_t)(s2 * 2)};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)box2};
+    cuuint64_t strides[2] = {(cuuint64_t)(s1 * esz), (cuuint64_t)(s2 * esz)};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / esz), 1, (cuuint32_t)box2};
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS && debug_on())
         fprintf(stderr, "[fprefill] tensor map dims (128,%lld,%lld) strides (%lld,%lld) box2 %d: CUresult %d\n",
-                n1, n2, s1 * 2, s2 * 2, box2, (int)r);
+                n1, n2, s1 * esz, s2 * esz, box2, (int)r);
     return r == CUDA_SUCCESS;
 }
 
@@ -563,10 +644,11 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     CUtensorMap tmQ, tmK, tmV, tmKm, tmVm;
     const long long total_q = bd.total_q;
     const long long tokens = (long long)L.num_pages * L.page_size;
-    if (!make_map(&tmQ, L.q, bd.h_q, total_q, L.q_stride_head, L.q_stride_tok, kBlock)) return fail("Q map", 0);
-    if (!make_map(&tmK, L.k_cache, bd.h_kv, tokens, kHeadDim, (long long)bd.h_kv * kHeadDim, rpb))
+    const bool f8 = L.fp8;
+    if (!make_map(&tmQ, L.q, bd.h_q, total_q, L.q_stride_head, L.q_stride_tok, kBlock, f8)) return fail("Q map", 0);
+    if (!make_map(&tmK, L.k_cache, bd.h_kv, tokens, kHeadDim, (long long)bd.h_kv * kHeadDim, rpb, f8))
         return fail("K map", 0);
-    if (!make_map(&tmV, L.v_cache, bd.h_kv, tokens, kHeadDim, (long long)bd.h_kv * kHeadDim, rpb))
+    if (!make_map(&tmV, L.v_cache, bd.h_kv, tokens, kHeadDim, (long long)bd.h_kv * kHeadDim, rpb, f8))
         return fail("V map", 0);
     const bool use_means = sparse && L.mean_corr;
     cudaError_t e;
@@ -574,11 +656,15 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
         // rows past the last block (padding up to one full 128-row box) are zero
         const long long n = (long long)bd.total_kb * bd.h_kv * kHeadDim;
         const long long n_pad = (long long)mean_rows(bd) * bd.h_kv * kHeadDim;
-        to_bf16_kernel<<<1024, 256, 0, st>>>(L.k_mean, L.v_mean, L.km16, L.vm16, n, n_pad);
-        if ((e = cudaGetLastError()) != cudaSuccess) return fail("to_bf16 launch", (int)e);
-        if (!make_map(&tmKm, L.km16, bd.h_kv, mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock))
+        if (f8)
+            to_e4m3_kernel<<<1024, 256, 0, st>>>(L.k_mean, L.v_mean, L.k_scale, L.v_scale, (uint8_t *)L.km16,
+                                                 (uint8_t *)L.vm16, n, n_pad, bd.h_kv);
+        else
+            to_bf16_kernel<<<1024, 256, 0, st>>>(L.k_mean, L.v_mean, L.km16, L.vm16, n, n_pad);
+        if ((e = cudaGetLastError()) != cudaSuccess) return fail("mean conversion launch", (int)e);
+        if (!make_map(&tmKm, L.km16, bd.h_kv, mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock, f8))
             return fail("mean K map", 0);
-        if (!make_map(&tmVm, L.vm16, bd.h_kv, mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock))
+        if (!make_map(&tmVm, L.vm16, bd.h_kv, mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock, f8))
             return fail("mean V map", 0);
     } else {
         tmKm = tmK;     // never read
@@ -597,14 +683,17 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     a.n_pairs = n_pairs;
     a.mean_corr = use_means ? 1 : 0;
     a.scale_log2 = L.softmax_scale * 1.4426950408889634f;
+    a.q_scale = L.q_scale;
+    a.k_scale = L.k_scale;
+    a.v_scale = L.v_scale;
     a.out = (__nv_bfloat16 *)L.out;
     a.lse = L.lse;
     a.status = L.status;
     a.wait_ns = L.wait_ns;
-    if ((e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttn)) !=
-        cudaSuccess)
+    auto kern = f8 ? attn_kernel<true> : attn_kernel<false>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttn)) != cudaSuccess)
         return fail("attention smem attribute", (int)e);
-    attn_kernel<<<units, kAttnThreads, kSmemAttn, st>>>(bd, tmQ, tmK, tmV, tmKm, tmVm, a);
+    kern<<<units, kAttnThreads, kSmemAttn, st>>>(bd, tmQ, tmK, tmV, tmKm, tmVm, a);
     if ((e = cudaGetLastError()) != cudaSuccess) {
         if (debug_on()) fprintf(stderr, "[fprefill] attention launch: %s\n", cudaGetErrorString(e));
         return fail("attention launch", (int)e);

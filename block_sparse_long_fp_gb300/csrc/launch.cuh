@@ -17,6 +17,7 @@ size_t score_smem_bytes(int max_nkb);
 // tensor-core score map (bf16 inputs): the three bf16 terms of the means live in
 // a workspace of score_tc_terms_bytes()
 int score_tc_rows_pad(const BatchDesc &bd);
+size_t score_tc_smem_bytes(int max_nkb);   // the tensor-core path needs this <= 227 KB
 inline size_t score_tc_terms_bytes(const BatchDesc &bd) {
     return (size_t)3 * score_tc_rows_pad(bd) * bd.h_kv * kHeadDim * 2;
 }
@@ -40,8 +41,10 @@ struct AttnLaunch {
     float *lse;
     int *status;
     int *work;
-    __nv_bfloat16 *km16, *vm16;
+    __nv_bfloat16 *km16, *vm16;       // block-mean copies (bf16, or e4m3 in the same space)
     unsigned long long wait_ns;
+    bool fp8;                         // e4m3 q / k / v with per-head scales
+    const float *q_scale, *k_scale, *v_scale;
 };
 int launch_attn(const AttnLaunch &L, cudaStream_t st);
 // rows of the bf16 block-mean copies: at least one full 128-row TMA box

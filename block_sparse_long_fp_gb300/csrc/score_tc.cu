@@ -9,16 +9,18 @@
 // significant bits, like fp32); Q is exactly representable in bf16 (and e4m3
 // inputs would be too, but those use the fp32 CUDA-core kernel).
 //
-// One CTA per score row (request, query block I, kv head h):
-//   for each query head of the group (128-query tile, M = 128):
-//     pass 0: S = Q Kmean^T over the row's key blocks 0..I, 64 at a time -> row max
-//     pass 1: the same S again -> exp2((s - max) * scale * log2 e), summed down
-//             the 128 queries (a transpose-reduce across each warp's 32 rows)
-//             and accumulated into the score row in global memory;
-//   finally the row is divided by its maximum.
-// Warp 0 issues TMA loads (Q per head, the three mean terms per 64-block
-// chunk, 3-stage ring), warp 1 issues the MMAs into four 64-column TMEM
-// buffers, warps 4-7 read S from TMEM (one query row per thread).
+// One CTA per score row (request, query block I, kv head h).  The g query
+// heads of the group go in pairs (A, B), each head a 128-query tile (M = 128):
+//   pass 0: S = Q Kmean^T over the row's key blocks 0..I, 64 at a time -> row max
+//   pass 1: the same S again -> exp2((s - max) * scale * log2 e), summed down
+//           the 128 queries (a transpose-reduce across each warp's 32 rows)
+//           into per-warp column sums in shared memory;
+// then S' = the sum of all warps' column sums (fixed order) and the row is
+// divided by its maximum.  Warp 0 issues TMA loads (Q of a head pair; the
+// three mean terms of a 64-block chunk, shared by both heads, in a 2-stage
+// ring), warp 1 issues the MMAs, warpgroup A (warps 4-7) and warpgroup B
+// (warps 8-11) each own one head of the pair and two 64-column TMEM buffers,
+// one query row per thread, so the two heads' row work overlaps.
 #include "common.cuh"
 #include "launch.cuh"
 #include "sm100.cuh"
@@ -29,36 +31,37 @@ using namespace sm100;
 
 namespace {
 
-constexpr int kScThreads = 256;
+constexpr int kScThreads = 384;
 constexpr int kChunk = 64;                                 // key blocks per chunk (MMA N)
 constexpr int kQBytes = kBlock * kHeadDim * 2;             // 32 KB
 constexpr int kTermBytes = kChunk * kHeadDim * 2;          // 16 KB: one term of one chunk
 constexpr int kStageBytes = 3 * kTermBytes;                // 48 KB
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int kTmemBufs = 4;
 constexpr int kSmQ = 0;
 constexpr int kSmStage = 2 * kQBytes;                      // 64 KB
-constexpr int kSmPart = kSmStage + kStages * kStageBytes;  // 208 KB
-constexpr int kSmCtl = kSmPart + 2 * 4 * kChunk * 4;       // + 2 KB partial sums
-constexpr int kScoreTcSmem = kSmCtl + 256 + 1024;
+constexpr int kSmCtl = kSmStage + kStages * kStageBytes;   // 160 KB
+constexpr int kSmAcc = kSmCtl + 256;                       // per-warp column sums [8][max_nkb]
 
-enum { B_QF = 0, B_QE = 2, B_SF = 4, B_SE = 7, B_TF = 10, B_TE = 14, B_N = 18 };
+// barriers: Q full/empty per head slot, stage full/empty, TMEM full/empty per (slot, buffer)
+enum { B_QF = 0, B_QE = 2, B_SF = 4, B_SE = 6, B_TF = 8, B_TE = 12, B_N = 16 };
 
 struct ScoreTcArgs {
     float *score;
     float scale_log2;
     int rows_pad;             // rows of each mean term in the split array
+    int acc_stride;           // floats per warp accumulator (>= the row length)
     int *status;
     unsigned long long wait_ns;
 };
 
-// A barrier among the four row warps that cannot hang: each warp's lane 0
+// A barrier among the eight row warps that cannot hang: each warp's lane 0
 // adds one arrival to a shared counter and spins (bounded, like the mbarrier
-// waits) until all four warps of this generation have arrived.  Returns false
+// waits) until all eight warps of this generation have arrived.  Returns false
 // if the CTA is aborting.
 __device__ __forceinline__ bool rows_sync(unsigned *ctr, unsigned &gen, int lane, volatile int *abort_flag,
                                           int *status, unsigned long long wait_ns) {
-    gen += 4;
+    gen += 8;
     bool ok = true;
     __threadfence_block();          // this lane's shared / global writes before the arrival
     __syncwarp();
@@ -126,12 +129,12 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                 const __grid_constant__ CUtensorMap tmM, const ScoreTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *part = reinterpret_cast<float *>(smem + kSmPart);            // [2][4 warps][64]
+    float *acc = reinterpret_cast<float *>(smem + kSmAcc);              // [4 warps][acc_stride]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmCtl);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kSmCtl + B_N * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kSmCtl + B_N * 8 + 4);
-    float *red = reinterpret_cast<float *>(smem + kSmCtl + B_N * 8 + 16);   // [4]
-    unsigned *sync_ctr = reinterpret_cast<unsigned *>(smem + kSmCtl + B_N * 8 + 32);
+    float *red = reinterpret_cast<float *>(smem + kSmCtl + B_N * 8 + 16);   // [8]
+    unsigned *sync_ctr = reinterpret_cast<unsigned *>(smem + kSmCtl + B_N * 8 + 48);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t sbase = smem_u32(smem);
@@ -149,8 +152,11 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
     const int g = bd.g;
     float *out = a.score + score_row_offset(rq, bd.h_kv, il, h);
 
+    const int npairs = (g + 1) / 2;
+    const int steps_per_pair = 2 * nch;
+
     if (threadIdx.x == 0) {
-        for (int k = 0; k < B_N; ++k) mbar_init(bar(k), (k >= B_TE && k < B_TE + kTmemBufs) ? 128u : 1u);
+        for (int k = 0; k < B_N; ++k) mbar_init(bar(k), (k >= B_TE && k < B_TE + 4) ? 128u : 1u);
         *abort_flag = 0;
         *sync_ctr = 0u;
         fence_barrier_init();
@@ -170,28 +176,30 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmM);
-            int item = 0;
-            for (int hh = 0; hh < g && !*abort_flag; ++hh) {
-                const int qb = hh & 1;
-                if (hh >= 2 && !mbar_wait(bar(B_QE + qb), ((hh >> 1) - 1) & 1, abort_flag, a.status, a.wait_ns))
-                    break;
-                mbar_expect_tx(bar(B_QF + qb), kQBytes);
-                for (int hf = 0; hf < 2; ++hf)
-                    tma_load_3d(sbase + kSmQ + qb * kQBytes + hf * (kQBytes / 2), &tmQ, bar(B_QF + qb), hf * 64,
-                                h * g + hh, rq.q_off + il * kBlock);
-                for (int pass = 0; pass < 2; ++pass)
-                    for (int c = 0; c < nch; ++c, ++item) {
-                        const int s = item % kStages, use = item / kStages;
-                        if (item >= kStages &&
-                            !mbar_wait(bar(B_SE + s), (use - 1) & 1, abort_flag, a.status, a.wait_ns))
-                            goto producer_done;
-                        mbar_expect_tx(bar(B_SF + s), kStageBytes);
-                        const uint32_t dst = sbase + kSmStage + s * kStageBytes;
-                        for (int t = 0; t < 3; ++t)
-                            for (int hf = 0; hf < 2; ++hf)
-                                tma_load_3d(dst + t * kTermBytes + hf * (kTermBytes / 2), &tmM, bar(B_SF + s),
-                                            hf * 64, h, t * a.rows_pad + rq.kb_base + c * kChunk);
-                    }
+            int step = 0;
+            for (int pr = 0; pr < npairs && !*abort_flag; ++pr) {
+                for (int w = 0; w < 2; ++w) {
+                    const int hh = 2 * pr + w;
+                    if (hh >= g) break;
+                    if (pr >= 1 && !mbar_wait(bar(B_QE + w), (pr - 1) & 1, abort_flag, a.status, a.wait_ns))
+                        goto producer_done;
+                    mbar_expect_tx(bar(B_QF + w), kQBytes);
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_load_3d(sbase + kSmQ + w * kQBytes + hf * (kQBytes / 2), &tmQ, bar(B_QF + w), hf * 64,
+                                    h * g + hh, rq.q_off + il * kBlock);
+                }
+                for (int k = 0; k < steps_per_pair; ++k, ++step) {
+                    const int c = k % nch;
+                    const int s = step % kStages, use = step / kStages;
+                    if (step >= kStages && !mbar_wait(bar(B_SE + s), (use - 1) & 1, abort_flag, a.status, a.wait_ns))
+                        goto producer_done;
+                    mbar_expect_tx(bar(B_SF + s), kStageBytes);
+                    const uint32_t dst = sbase + kSmStage + s * kStageBytes;
+                    for (int t = 0; t < 3; ++t)
+                        for (int hf = 0; hf < 2; ++hf)
+                            tma_load_3d(dst + t * kTermBytes + hf * (kTermBytes / 2), &tmM, bar(B_SF + s), hf * 64, h,
+                                        t * a.rows_pad + rq.kb_base + c * kChunk);
+                }
             }
         producer_done:;
         }
@@ -199,66 +207,76 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
         // ================= MMA issuer =================
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16(128, kChunk, false);
-            int item = 0;
-            for (int hh = 0; hh < g; ++hh) {
-                const int qb = hh & 1;
-                if (!mbar_wait(bar(B_QF + qb), (hh >> 1) & 1, abort_flag, a.status, a.wait_ns)) goto mma_done;
-                const uint32_t qa = sbase + kSmQ + qb * kQBytes;
-                for (int pass = 0; pass < 2; ++pass)
-                    for (int c = 0; c < nch; ++c, ++item) {
-                        const int s = item % kStages, b = item % kTmemBufs;
-                        if (!mbar_wait(bar(B_SF + s), (item / kStages) & 1, abort_flag, a.status, a.wait_ns))
-                            goto mma_done;
-                        if (item >= kTmemBufs &&
-                            !mbar_wait(bar(B_TE + b), ((item / kTmemBufs) - 1) & 1, abort_flag, a.status,
-                                       a.wait_ns))
+            int step = 0;
+            int uses[2] = {0, 0};                  // TMEM-buffer uses per head slot
+            for (int pr = 0; pr < npairs; ++pr) {
+                const int nw = (2 * pr + 1 < g) ? 2 : 1;
+                for (int w = 0; w < nw; ++w)
+                    if (!mbar_wait(bar(B_QF + w), pr & 1, abort_flag, a.status, a.wait_ns)) goto mma_done;
+                for (int k = 0; k < steps_per_pair; ++k, ++step) {
+                    const int s = step % kStages;
+                    if (!mbar_wait(bar(B_SF + s), (step / kStages) & 1, abort_flag, a.status, a.wait_ns)) goto mma_done;
+                    const uint32_t kb = sbase + kSmStage + s * kStageBytes;
+                    for (int w = 0; w < nw; ++w) {
+                        const int u = uses[w]++;
+                        const int b = u & 1;
+                        if (u >= 2 && !mbar_wait(bar(B_TE + 2 * w + b), ((u >> 1) - 1) & 1, abort_flag, a.status,
+                                                 a.wait_ns))
                             goto mma_done;
                         tc_fence_after();
-                        const uint32_t kb = sbase + kSmStage + s * kStageBytes;
+                        // descriptors differ only in the start address: add offsets (in 16-byte units)
+                        const uint64_t qd = smem_desc_sw128(sbase + kSmQ + w * kQBytes, 16, 1024);
+                        const uint64_t kd = smem_desc_sw128(kb, 16, 1024);
+                        const uint32_t dt = tmem + (2 * w + b) * kChunk;
 #pragma unroll
                         for (int t = 0; t < 3; ++t)
 #pragma unroll
                             for (int kk = 0; kk < kHeadDim / 16; ++kk) {
                                 const uint32_t off = (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32;
                                 const uint32_t boff = t * kTermBytes + (kk >> 2) * (kTermBytes / 2) + (kk & 3) * 32;
-                                mma_ss(tmem + b * kChunk, smem_desc_sw128(qa + off, 16, 1024),
-                                       smem_desc_sw128(kb + boff, 16, 1024), idS, (t | kk) != 0);
+                                mma_ss(dt, qd + (off >> 4), kd + (boff >> 4), idS, (t | kk) != 0);
                             }
-                        tc_commit(bar(B_TF + b));
-                        tc_commit(bar(B_SE + s));
+                        tc_commit(bar(B_TF + 2 * w + b));
                     }
-                tc_commit(bar(B_QE + qb));
+                    tc_commit(bar(B_SE + s));
+                }
+                for (int w = 0; w < nw; ++w) tc_commit(bar(B_QE + w));
             }
         mma_done:;
         }
     } else if (warp >= 4) {
-        // ================= row warpgroup: one query row per thread =================
-        const int quarter = warp - 4;
+        // ================= row warpgroups: one head each, one query row per thread =================
+        const int w = (warp - 4) / 4;                     // head slot of the pair
+        const int quarter = warp % 4;
         const int rowt = quarter * 32 + lane;
         const bool row_valid = il * kBlock + rowt < rq.lq;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        int item = 0;
+        float *my_acc = acc + (w * 4 + quarter) * a.acc_stride;   // this warp's 32 rows, summed
+        for (int J = lane; J < ncol; J += 32) my_acc[J] = 0.f;
+        __syncwarp();
+        int u = 0;
         bool ok = true;
         unsigned gen = 0;
-        for (int hh = 0; hh < g && ok; ++hh) {
-            const float c2 = a.scale_log2;
+        const float c2 = a.scale_log2;
+        for (int pr = 0; pr < npairs && ok; ++pr) {
+            if (2 * pr + w >= g) break;
             float m = -INFINITY;
             float mc2 = 0.f;
             for (int pass = 0; pass < 2 && ok; ++pass) {
                 if (pass == 1) mc2 = (m == -INFINITY || !row_valid) ? 0.f : m * c2;
-                for (int c = 0; c < nch; ++c, ++item) {
-                    const int b = item % kTmemBufs;
-                    const bool got = mbar_wait(bar(B_TF + b), (item / kTmemBufs) & 1, abort_flag, a.status, a.wait_ns);
+                for (int c = 0; c < nch; ++c, ++u) {
+                    const int b = u & 1;
+                    const bool got = mbar_wait(bar(B_TF + 2 * w + b), (u >> 1) & 1, abort_flag, a.status, a.wait_ns);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     tc_fence_after();
                     uint32_t u0[32], u1[32];
-                    tmem_ld32(lane_base + b * kChunk, u0);
-                    tmem_ld32(lane_base + b * kChunk + 32, u1);
+                    tmem_ld32(lane_base + (2 * w + b) * kChunk, u0);
+                    tmem_ld32(lane_base + (2 * w + b) * kChunk + 32, u1);
                     tmem_ld_wait();
                     reg_fence(u0);
                     reg_fence(u1);
                     tc_fence_before();
-                    mbar_arrive(bar(B_TE + b));
+                    mbar_arrive(bar(B_TE + 2 * w + b));
                     const int J0 = c * kChunk;
                     if (pass == 0) {
                         float m4[4] = {m, -INFINITY, -INFINITY, -INFINITY};
@@ -277,37 +295,37 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                         }
                         const float s0 = transpose_reduce32(v0, lane);
                         const float s1 = transpose_reduce32(v1, lane);
-                        float *pp = part + (item & 1) * 4 * kChunk + quarter * kChunk;
-                        pp[lane] = s0;
-                        pp[32 + lane] = s1;
-                        if (!rows_sync(sync_ctr, gen, lane, abort_flag, a.status, a.wait_ns)) { ok = false; break; }
-                        const int t = threadIdx.x - 128;
-                        if (t < kChunk && J0 + t < ncol) {
-                            const float *q = part + (item & 1) * 4 * kChunk;
-                            const float v = (q[t] + q[kChunk + t]) + (q[2 * kChunk + t] + q[3 * kChunk + t]);
-                            out[J0 + t] = hh == 0 ? v : out[J0 + t] + v;
-                        }
+                        // lane L now holds the sums of columns J0 + L and J0 + 32 + L
+                        if (J0 + lane < ncol) my_acc[J0 + lane] += s0;
+                        if (J0 + 32 + lane < ncol) my_acc[J0 + 32 + lane] += s1;
                     }
                 }
             }
         }
-        // re-normalise the row by its maximum
+        // S' = the eight warps' sums (fixed order); re-normalise by its maximum
         if (ok) ok = rows_sync(sync_ctr, gen, lane, abort_flag, a.status, a.wait_ns);
         if (ok) {
             const int t = threadIdx.x - 128;
+            const int st = a.acc_stride;
+            auto colsum = [&](int J) {
+                return ((acc[J] + acc[st + J]) + (acc[2 * st + J] + acc[3 * st + J])) +
+                       ((acc[4 * st + J] + acc[5 * st + J]) + (acc[6 * st + J] + acc[7 * st + J]));
+            };
             float mx = 0.f;
-            for (int J = t; J < ncol; J += 128) mx = fmaxf(mx, out[J]);
+            for (int J = t; J < ncol; J += 256) mx = fmaxf(mx, colsum(J));
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (lane == 0) red[quarter] = mx;
-            if (!rows_sync(sync_ctr, gen, lane, abort_flag, a.status, a.wait_ns)) mx = 0.f;
-            mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+            if (lane == 0) red[warp - 4] = mx;
+            const bool ok2 = rows_sync(sync_ctr, gen, lane, abort_flag, a.status, a.wait_ns);
+            mx = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx = fmaxf(mx, red[k]);
             const float inv = 1.f / mx;
-            if (!*abort_flag)
-            for (int J = t; J < ncol; J += 128) {
-                const float v = out[J];
-                out[J] = v == mx ? 1.f : v * inv;
-            }
+            if (ok2)
+                for (int J = t; J < ncol; J += 256) {
+                    const float v = colsum(J);
+                    out[J] = v == mx ? 1.f : v * inv;
+                }
         }
     }
 
@@ -369,6 +387,8 @@ bool map3(CUtensorMap *m, const void *base, long long n1, long long n2, long lon
 
 int score_tc_rows_pad(const BatchDesc &bd) { return bd.total_kb > kChunk ? bd.total_kb : kChunk; }
 
+size_t score_tc_smem_bytes(int max_nkb) { return (size_t)kSmAcc + 8 * sizeof(float) * max_nkb + 1024; }
+
 cudaError_t launch_score_tc(const BatchDesc &bd, const void *q, long long q_stride_tok, long long q_stride_head,
                             const float *k_mean, float softmax_scale, float *score, __nv_bfloat16 *terms,
                             int *status, unsigned long long wait_ns, cudaStream_t st) {
@@ -386,11 +406,13 @@ cudaError_t launch_score_tc(const BatchDesc &bd, const void *q, long long q_stri
     a.score = score;
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
     a.rows_pad = rows_pad;
+    a.acc_stride = bd.max_nkb;
     a.status = status;
     a.wait_ns = wait_ns;
-    e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreTcSmem);
+    const int smem = (int)score_tc_smem_bytes(bd.max_nkb);
+    e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    score_tc_kernel<<<bd.total_rows, kScThreads, kScoreTcSmem, st>>>(bd, tmQ, tmM, a);
+    score_tc_kernel<<<bd.total_rows, kScThreads, smem, st>>>(bd, tmQ, tmM, a);
     return cudaGetLastError();
 }
 

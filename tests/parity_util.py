@@ -7,6 +7,9 @@ import numpy as np
 # tolerances of the output (against float64): bf16 path max-abs 2e-2, mean-abs 2e-3
 BF16_MAX_ABS, BF16_MEAN_ABS = 2e-2, 2e-3
 FP8_MAX_ABS = 6e-2
+# LSE with e4m3 weights: each weight is within 1/16 relative of its value, so
+# the sum is too, and ln(1 + 1/16) bounds the LSE error
+FP8_LSE_ABS = 0.0607
 SCORE_ABS = 2e-6          # scores lie in (0, 1]; fp32 evaluation error is ~1e-7
 
 
@@ -95,7 +98,7 @@ def oracle_outputs(case, ref, mean_corr, dense=False, rows_per_request=None, see
     return outs
 
 
-def check_outputs(case, g, oref, max_abs=BF16_MAX_ABS, mean_abs=BF16_MEAN_ABS):
+def check_outputs(case, g, oref, max_abs=BF16_MAX_ABS, mean_abs=BF16_MEAN_ABS, lse_abs=2e-2):
     errs, lerrs = [], []
     for r, (qi, qh, o, lse) in enumerate(oref):
         q0 = int(case.cu_seqlens_q[r])
@@ -105,9 +108,9 @@ def check_outputs(case, g, oref, max_abs=BF16_MAX_ABS, mean_abs=BF16_MEAN_ABS):
     e = np.concatenate(errs)
     le = np.concatenate(lerrs)
     assert np.isfinite(e).all()
-    assert e.max() <= max_abs, e.max()
+    assert e.max() <= max_abs, (e.max(), e.mean())
     assert e.mean() <= mean_abs, e.mean()
-    assert le.max() <= 2e-2, le.max()
+    assert le.max() <= lse_abs, le.max()
     return float(e.max()), float(e.mean())
 
 
