@@ -96,11 +96,11 @@ float softmax_scale_of(const fp_params *prm, int d) {
 
 int *status_ptr(void *ws) { return reinterpret_cast<int *>(ws); }
 
-// bf16 scores run on the tensor cores while their per-warp column sums fit in
-// shared memory (rows up to 4096 key blocks); e4m3 and longer rows use the
-// fp32 CUDA-core kernel.
+// Scores run on the tensor cores while the per-warp column sums fit in shared
+// memory (rows up to 2048 key blocks); longer rows use the fp32 CUDA-core kernel.
 bool use_score_tc(const fp_problem *p, const BatchDesc &bd) {
-    return p->dtype == FP_BF16 && score_tc_smem_bytes(bd.max_nkb) <= 227 * 1024;
+    (void)p;
+    return score_tc_smem_bytes(bd.max_nkb) <= 227 * 1024;
 }
 
 size_t attn_ws_bytes(const BatchDesc &bd) {
@@ -173,8 +173,8 @@ fp_status fp_discover(const fp_problem *p, const fp_params *prm, float *k_mean, 
             e = launch_score(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean,
                              softmax_scale_of(prm, p->d), score, st);
         else
-            e = launch_score_tc(bd, p->q, p->q_stride_tok, p->q_stride_head, k_mean, softmax_scale_of(prm, p->d),
-                                score,
+            e = launch_score_tc(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean,
+                                softmax_scale_of(prm, p->d), score,
                                 reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + kWsHeaderBytes),
                                 status_ptr(ws), g_wait_ns, st);
         if (e != cudaSuccess) return FP_ERR_CUDA;

@@ -21,9 +21,10 @@ size_t score_tc_smem_bytes(int max_nkb);   // the tensor-core path needs this <=
 inline size_t score_tc_terms_bytes(const BatchDesc &bd) {
     return (size_t)3 * score_tc_rows_pad(bd) * bd.h_kv * kHeadDim * 2;
 }
-cudaError_t launch_score_tc(const BatchDesc &bd, const void *q, long long q_stride_tok, long long q_stride_head,
-                            const float *k_mean, float softmax_scale, float *score, __nv_bfloat16 *terms,
-                            int *status, unsigned long long wait_ns, cudaStream_t st);
+cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
+                            long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
+                            float *score, __nv_bfloat16 *terms, int *status, unsigned long long wait_ns,
+                            cudaStream_t st);
 
 struct AttnLaunch {
     const BatchDesc *bd;

@@ -49,6 +49,9 @@ enum { B_QF = 0, B_QE = 2, B_SF = 4, B_SE = 6, B_TF = 8, B_TE = 12, B_N = 16 };
 struct ScoreTcArgs {
     float *score;
     float scale_log2;
+    const uint8_t *q8;        // e4m3 only: query codes, strides in elements (bytes)
+    long long q_stride_tok, q_stride_head;
+    const float *q_scale;     // e4m3 only: per query head
     int rows_pad;             // rows of each mean term in the split array
     int acc_stride;           // floats per warp accumulator (>= the row length)
     int *status;
@@ -85,6 +88,11 @@ __device__ __forceinline__ bool rows_sync(unsigned *ctr, unsigned &gen, int lane
     __threadfence_block();          // the other warps' writes are visible from here on
     ok = __shfl_sync(0xffffffffu, ok, 0);
     return ok;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
 }
 
 // Column sums of a 32x32 block held one row per lane (v[c] = column c of
@@ -124,6 +132,10 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
     return keep + __shfl_xor_sync(0xffffffffu, send, 1);
 }
 
+// kFp8: the query tiles are e4m3 codes; each row warpgroup loads its rows,
+// converts them exactly to bf16 and writes the swizzled tile itself (the
+// mean terms are bf16 either way), and the head's scale joins the exponent.
+template <bool kFp8>
 __global__ void __launch_bounds__(kScThreads, 1)
 score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmM, const ScoreTcArgs a) {
@@ -156,7 +168,8 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
     const int steps_per_pair = 2 * nch;
 
     if (threadIdx.x == 0) {
-        for (int k = 0; k < B_N; ++k) mbar_init(bar(k), (k >= B_TE && k < B_TE + 4) ? 128u : 1u);
+        for (int k = 0; k < B_N; ++k)
+            mbar_init(bar(k), ((k >= B_TE && k < B_TE + 4) || (kFp8 && k >= B_QF && k < B_QF + 2)) ? 128u : 1u);
         *abort_flag = 0;
         *sync_ctr = 0u;
         fence_barrier_init();
@@ -178,7 +191,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
             tma_prefetch_desc(&tmM);
             int step = 0;
             for (int pr = 0; pr < npairs && !*abort_flag; ++pr) {
-                for (int w = 0; w < 2; ++w) {
+                for (int w = 0; w < 2 && !kFp8; ++w) {
                     const int hh = 2 * pr + w;
                     if (hh >= g) break;
                     if (pr >= 1 && !mbar_wait(bar(B_QE + w), (pr - 1) & 1, abort_flag, a.status, a.wait_ns))
@@ -257,9 +270,43 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
         int u = 0;
         bool ok = true;
         unsigned gen = 0;
-        const float c2 = a.scale_log2;
         for (int pr = 0; pr < npairs && ok; ++pr) {
             if (2 * pr + w >= g) break;
+            const int hq = h * g + 2 * pr + w;
+            const float c2 = kFp8 ? a.scale_log2 * __ldg(a.q_scale + hq) : a.scale_log2;
+            if constexpr (kFp8) {
+                // this head's 128 query rows -> bf16 (exact), 128-byte swizzled K-major tile
+                if (pr >= 1) {
+                    const bool got = mbar_wait(bar(B_QE + w), (pr - 1) & 1, abort_flag, a.status, a.wait_ns);
+                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                }
+                uint8_t *qt = smem + kSmQ + w * kQBytes;
+                const int qi = il * kBlock + rowt;
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    a.q8 + (long long)(rq.q_off + qi) * a.q_stride_tok + (long long)hq * a.q_stride_head);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {                      // 16 codes per 16-byte load
+                    const uint4 c16 = row_valid ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                    const uint32_t cw[4] = {c16.x, c16.y, c16.z, c16.w};
+#pragma unroll
+                    for (int half8 = 0; half8 < 2; ++half8) {      // 8 codes -> one 16-byte bf16 chunk
+                        uint32_t o[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t word = cw[half8 * 2 + k / 2];
+                            const __nv_fp8x2_storage_t c2v = (__nv_fp8x2_storage_t)(word >> (16 * (k & 1)));
+                            const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(c2v, __NV_E4M3)));
+                            o[k] = pack_bf16x2(f.x, f.y);
+                        }
+                        const int col = v * 16 + half8 * 8;           // first of the 8 columns
+                        const int hf = col >> 6, j = (col & 63) >> 3;
+                        *reinterpret_cast<uint4 *>(qt + hf * (kQBytes / 2) + rowt * 128 + ((j ^ (rowt & 7)) << 4)) =
+                            make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+                fence_proxy_async();                               // visible to the tensor core
+                mbar_arrive(bar(B_QF + w));
+            }
             float m = -INFINITY;
             float mc2 = 0.f;
             for (int pass = 0; pass < 2 && ok; ++pass) {
@@ -389,9 +436,10 @@ int score_tc_rows_pad(const BatchDesc &bd) { return bd.total_kb > kChunk ? bd.to
 
 size_t score_tc_smem_bytes(int max_nkb) { return (size_t)kSmAcc + 8 * sizeof(float) * max_nkb + 1024; }
 
-cudaError_t launch_score_tc(const BatchDesc &bd, const void *q, long long q_stride_tok, long long q_stride_head,
-                            const float *k_mean, float softmax_scale, float *score, __nv_bfloat16 *terms,
-                            int *status, unsigned long long wait_ns, cudaStream_t st) {
+cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
+                            long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
+                            float *score, __nv_bfloat16 *terms, int *status, unsigned long long wait_ns,
+                            cudaStream_t st) {
     const int rows_pad = score_tc_rows_pad(bd);
     const long long n = (long long)bd.total_kb * bd.h_kv * kHeadDim;
     const long long n_pad = (long long)rows_pad * bd.h_kv * kHeadDim;
@@ -399,20 +447,26 @@ cudaError_t launch_score_tc(const BatchDesc &bd, const void *q, long long q_stri
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap tmQ, tmM;
-    if (!map3(&tmQ, q, bd.h_q, bd.total_q, q_stride_head, q_stride_tok, kBlock)) return cudaErrorInvalidValue;
+    if (!fp8 && !map3(&tmQ, q, bd.h_q, bd.total_q, q_stride_head, q_stride_tok, kBlock)) return cudaErrorInvalidValue;
     if (!map3(&tmM, terms, bd.h_kv, 3LL * rows_pad, kHeadDim, (long long)bd.h_kv * kHeadDim, kChunk))
         return cudaErrorInvalidValue;
     ScoreTcArgs a;
     a.score = score;
+    a.q8 = (const uint8_t *)q;
+    a.q_stride_tok = q_stride_tok;
+    a.q_stride_head = q_stride_head;
+    a.q_scale = q_scale;
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
     a.rows_pad = rows_pad;
     a.acc_stride = bd.max_nkb;
     a.status = status;
     a.wait_ns = wait_ns;
+    if (fp8) tmQ = tmM;                  // not read: the row warps load e4m3 queries themselves
     const int smem = (int)score_tc_smem_bytes(bd.max_nkb);
-    e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto kern = fp8 ? score_tc_kernel<true> : score_tc_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    score_tc_kernel<<<bd.total_rows, kScThreads, smem, st>>>(bd, tmQ, tmM, a);
+    kern<<<bd.total_rows, kScThreads, smem, st>>>(bd, tmQ, tmM, a);
     return cudaGetLastError();
 }
 

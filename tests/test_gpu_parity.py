@@ -199,3 +199,28 @@ def test_fp8_attention_sharp_varlen(mean_corr):
     r = full_parity(spec, mean_corr=mean_corr, rows_per_request=2000, max_abs=0.1, mean_abs=6e-3,
                     lse_abs=FP8_LSE_ABS)
     assert r["density"] < 0.95
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_rows_longer_than_2048_blocks_use_the_fp32_score_kernel(dtype):
+    """A 262,272-token request (2049 key blocks) is past the tensor-core score
+    kernel's shared-memory limit: its scores come from the fp32 CUDA-core
+    kernel.  Sampled score rows and their index rows against the oracle."""
+    import oracle
+    import torch
+    from block_sparse_long_fp_gb300 import fprefill
+    L = 2049 * 128
+    spec = synth.Spec("long-rows", [(L, 0)], 2, 1, page_size=128, layout="shuffled", dtype=dtype,
+                      n_needles=2, logit_scale=4.0, config_id=77)
+    case = synth.make_case(spec)
+    rows = np.array([0, 5, 700, 2047, 2048])
+    ref = oracle.discover_and_select(case, row_subset=lambda r, nqb, hkv: rows)
+    layer = fprefill.layer_from_case(case)
+    k_mean, v_mean, score = layer.discover()
+    row_ptr, col_idx, nnz = layer.select(score)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    g = dict(k_mean=k_mean.cpu().numpy(), v_mean=v_mean.cpu().numpy(), score=score.cpu().numpy(),
+             row_ptr=row_ptr.cpu().numpy(), col_idx=col_idx.cpu().numpy())
+    check_pool(case, g, ref)
+    check_scores_and_index(case, g, ref)
