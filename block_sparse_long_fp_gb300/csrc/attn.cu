@@ -319,6 +319,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             const uint32_t tS = lane_base + t * 256;
             const uint32_t tO = tS + 128;
             float m = -INFINITY, l = 0.f;
+            const int last_J = n_kept == 0 ? -1 : (sparse ? __ldg(a.col_idx + rp0 + n_kept - 1) : n_kept - 1);
             bool ok = true;
             // logit scale (log2 units): e4m3 codes carry the per-head scales
             const float csc = kFp8 ? a.scale_log2 * __ldg(a.q_scale + hq0 + t) * __ldg(a.k_scale + h) : a.scale_log2;
@@ -346,8 +347,9 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]);
                 float bias = 0.f;
                 if (j < n_kept) {
-                    const int J = sparse ? __ldg(a.col_idx + rp0 + j) : j;
-                    const int k0 = J * kBlock;
+                    // kept blocks ascend and J <= I: only the last one can be the
+                    // diagonal block, the one that needs the causal mask
+                    const int k0 = j == n_kept - 1 ? last_J * kBlock : 0;
                     if (k0 + kBlock - 1 > pos) {          // the diagonal block: causal mask
 #pragma unroll
                         for (int e = 0; e < 128; ++e)
