@@ -138,6 +138,23 @@ class ClockSampler:
 # our arm
 # ----------------------------------------------------------------------------
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time (every rank calls this; a no-op at world 1)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(flop_per_replica: float, ms: float, world: int) -> float:
+    """Dense-equivalent TFLOP/s of the whole job: every rank runs one replica
+    of the layer (weak scaling), and the job takes the slowest rank's time."""
+    return world * flop_per_replica / (ms * 1e-3) / 1e12
+
+
 def cuda_time(fn, steps, stream):
     import torch
     a = torch.cuda.Event(enable_timing=True)
@@ -237,9 +254,7 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     clocks = clk.summary()
 
     # --- per-stage breakdown, the attention kernel alone, the dense path ---
@@ -276,7 +291,7 @@ def run_ours(args, rank, world):
     attn_flop = stats["kept_flop"] + stats["corr_flop"]
     achieved = attn_flop / (ms_attn * 1e-3) / 1e12
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    value = world * flop / (ms * 1e-3) / 1e12
+    value = whole_job_value(flop, ms, world)
     q_bytes = spec.total_q * spec.h_q * spec.d * 2
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,

@@ -1,4 +1,4 @@
-// Block-score map on tcgen05 tensor cores (bf16 inputs).
+// Block-score map on tcgen05 tensor cores.
 //
 // The scores of the FlashPrefill V1 summary, section 3.1 (per packed query
 // row: logits against the pooled keys, normalised by the row's own maximum,
@@ -6,8 +6,8 @@
 // by its largest entry) decide, through a threshold, which blocks are kept.
 // Decisions must not move relative to the float64 definition, so the pooled
 // keys enter the MMA as three bf16 terms, kmean = hi + mid + lo (24
-// significant bits, like fp32); Q is exactly representable in bf16 (and e4m3
-// inputs would be too, but those use the fp32 CUDA-core kernel).
+// significant bits, like fp32); Q is exactly representable in bf16, and so are
+// e4m3 query codes, which the row warps convert.
 //
 // One CTA per score row (request, query block I, kv head h).  The g query
 // heads of the group go in pairs (A, B), each head a 128-query tile (M = 128):
@@ -16,11 +16,13 @@
 //           the 128 queries (a transpose-reduce across each warp's 32 rows)
 //           into per-warp column sums in shared memory;
 // then S' = the sum of all warps' column sums (fixed order) and the row is
-// divided by its maximum.  Warp 0 issues TMA loads (Q of a head pair; the
-// three mean terms of a 64-block chunk, shared by both heads, in a 2-stage
-// ring), warp 1 issues the MMAs, warpgroup A (warps 4-7) and warpgroup B
-// (warps 8-11) each own one head of the pair and two 64-column TMEM buffers,
-// one query row per thread, so the two heads' row work overlaps.
+// divided by its maximum.  Warp 0 issues TMA loads (the three mean terms of a
+// chunk of key blocks, shared by both heads, in a ring of stages), warp 1
+// issues the MMAs, warpgroup A (warps 4-7) and warpgroup B (warps 8-11) each
+// own one head of the pair and its TMEM S buffers, one query row per thread,
+// so the two heads' row work overlaps.  Each warpgroup also writes its head's
+// query tile into TMEM, where the MMA takes it as the A operand: the MMAs read
+// only the mean terms from shared memory.
 #include "common.cuh"
 #include "launch.cuh"
 #include "sm100.cuh"
@@ -32,24 +34,38 @@ using namespace sm100;
 namespace {
 
 constexpr int kScThreads = 384;
-constexpr int kChunk = 64;                                 // key blocks per chunk (MMA N)
 constexpr int kQBytes = kBlock * kHeadDim * 2;             // 32 KB
-constexpr int kTermBytes = kChunk * kHeadDim * 2;          // 16 KB: one term of one chunk
-constexpr int kStageBytes = 3 * kTermBytes;                // 48 KB
-constexpr int kStages = 2;
-constexpr int kTmemBufs = 4;
-constexpr int kSmQ = 0;
-constexpr int kSmStage = 2 * kQBytes;                      // 64 KB
-constexpr int kSmCtl = kSmStage + kStages * kStageBytes;   // 160 KB
-constexpr int kSmAcc = kSmCtl + 256;                       // per-warp column sums [8][max_nkb]
 
-// barriers: Q full/empty per head slot, stage full/empty, TMEM full/empty per (slot, buffer)
-enum { B_QF = 0, B_QE = 2, B_SF = 4, B_SE = 6, B_TF = 8, B_TE = 12, B_N = 16 };
+// Layout of one build of the kernel for a chunk of kChunk key blocks (MMA N):
+// 128-block chunks halve the MMA instructions per FLOP (measured 2.9 vs 4.0
+// ms at 128K) but leave room for per-warp column sums of rows up to 1024
+// blocks only; 64-block chunks take rows up to 2048 blocks.
+template <int C>
+struct ScoreCfg {
+    static constexpr int kChunk = C;
+    static constexpr int kBufs = C == 64 ? 2 : 1;              // TMEM S buffers per head slot
+    static constexpr int kTermBytes = C * kHeadDim * 2;        // one term of one chunk
+    static constexpr int kStageBytes = 3 * kTermBytes;
+    static constexpr int kStages = C == 64 ? 3 : 2;
+    static constexpr int kTmemBufs = 2 * kBufs;
+    static constexpr int kSmStage = 0;
+    static constexpr int kSmCtl = kSmStage + kStages * kStageBytes;
+    static constexpr int kSmAcc = kSmCtl + 256;                // per-warp column sums [8][max_nkb]
+    // TMEM: the S buffers (kBufs per head slot), then the two query tiles as
+    // MMA A operands (128 rows x 128 bf16 = 64 columns each)
+    static constexpr int kTmemQ = kTmemBufs * C;
+    // barriers: Q full/empty per head slot, stage full/empty, TMEM full/empty per (slot, buffer)
+    static constexpr int B_QF = 0, B_QE = 2, B_SF = 4, B_SE = 4 + kStages, B_TF = 4 + 2 * kStages;
+    static constexpr int B_TE = B_TF + 4, B_N = B_TE + 4;
+    static_assert(kTmemQ + 128 <= 512, "TMEM budget");
+    static size_t smem_bytes(int max_nkb) { return (size_t)kSmAcc + 8 * sizeof(float) * max_nkb + 1024; }
+};
 
 struct ScoreTcArgs {
     float *score;
     float scale_log2;
-    const uint8_t *q8;        // e4m3 only: query codes, strides in elements (bytes)
+    const uint8_t *q8;        // e4m3 queries (codes); strides in elements
+    const __nv_bfloat16 *q16; // bf16 queries
     long long q_stride_tok, q_stride_head;
     const float *q_scale;     // e4m3 only: per query head
     int rows_pad;             // rows of each mean term in the split array
@@ -135,10 +151,16 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
 // kFp8: the query tiles are e4m3 codes; each row warpgroup loads its rows,
 // converts them exactly to bf16 and writes the swizzled tile itself (the
 // mean terms are bf16 either way), and the head's scale joins the exponent.
-template <bool kFp8>
+template <bool kFp8, int kCh>
 __global__ void __launch_bounds__(kScThreads, 1)
 score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmM, const ScoreTcArgs a) {
+    using Cfg = ScoreCfg<kCh>;
+    constexpr int kChunk = Cfg::kChunk, kBufs = Cfg::kBufs, kTermBytes = Cfg::kTermBytes;
+    constexpr int kStageBytes = Cfg::kStageBytes, kStages = Cfg::kStages, kSmStage = Cfg::kSmStage;
+    constexpr int kSmCtl = Cfg::kSmCtl, kSmAcc = Cfg::kSmAcc, kTmemQ = Cfg::kTmemQ;
+    constexpr int B_QF = Cfg::B_QF, B_QE = Cfg::B_QE, B_SF = Cfg::B_SF, B_SE = Cfg::B_SE;
+    constexpr int B_TF = Cfg::B_TF, B_TE = Cfg::B_TE, B_N = Cfg::B_N;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *acc = reinterpret_cast<float *>(smem + kSmAcc);              // [4 warps][acc_stride]
@@ -169,14 +191,14 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < B_N; ++k)
-            mbar_init(bar(k), ((k >= B_TE && k < B_TE + 4) || (kFp8 && k >= B_QF && k < B_QF + 2)) ? 128u : 1u);
+            mbar_init(bar(k), ((k >= B_TE && k < B_TE + 4) || (k >= B_QF && k < B_QF + 2)) ? 128u : 1u);
         *abort_flag = 0;
         *sync_ctr = 0u;
         fence_barrier_init();
         fence_proxy_async();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -187,20 +209,9 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmM);
             int step = 0;
             for (int pr = 0; pr < npairs && !*abort_flag; ++pr) {
-                for (int w = 0; w < 2 && !kFp8; ++w) {
-                    const int hh = 2 * pr + w;
-                    if (hh >= g) break;
-                    if (pr >= 1 && !mbar_wait(bar(B_QE + w), (pr - 1) & 1, abort_flag, a.status, a.wait_ns))
-                        goto producer_done;
-                    mbar_expect_tx(bar(B_QF + w), kQBytes);
-                    for (int hf = 0; hf < 2; ++hf)
-                        tma_load_3d(sbase + kSmQ + w * kQBytes + hf * (kQBytes / 2), &tmQ, bar(B_QF + w), hf * 64,
-                                    h * g + hh, rq.q_off + il * kBlock);
-                }
                 for (int k = 0; k < steps_per_pair; ++k, ++step) {
                     const int c = k % nch;
                     const int s = step % kStages, use = step / kStages;
@@ -232,24 +243,23 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                     const uint32_t kb = sbase + kSmStage + s * kStageBytes;
                     for (int w = 0; w < nw; ++w) {
                         const int u = uses[w]++;
-                        const int b = u & 1;
-                        if (u >= 2 && !mbar_wait(bar(B_TE + 2 * w + b), ((u >> 1) - 1) & 1, abort_flag, a.status,
+                        const int b = u % kBufs;
+                        if (u >= kBufs && !mbar_wait(bar(B_TE + kBufs * w + b), ((u / kBufs) - 1) & 1, abort_flag, a.status,
                                                  a.wait_ns))
                             goto mma_done;
                         tc_fence_after();
                         // descriptors differ only in the start address: add offsets (in 16-byte units)
-                        const uint64_t qd = smem_desc_sw128(sbase + kSmQ + w * kQBytes, 16, 1024);
                         const uint64_t kd = smem_desc_sw128(kb, 16, 1024);
-                        const uint32_t dt = tmem + (2 * w + b) * kChunk;
+                        const uint32_t dt = tmem + (kBufs * w + b) * kChunk;
+                        const uint32_t qt = tmem + kTmemQ + w * 64;          // A: 16 d-values per 8 columns
 #pragma unroll
                         for (int t = 0; t < 3; ++t)
 #pragma unroll
                             for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                                const uint32_t off = (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32;
                                 const uint32_t boff = t * kTermBytes + (kk >> 2) * (kTermBytes / 2) + (kk & 3) * 32;
-                                mma_ss(dt, qd + (off >> 4), kd + (boff >> 4), idS, (t | kk) != 0);
+                                mma_ts(dt, qt + kk * 8, kd + (boff >> 4), idS, (t | kk) != 0);
                             }
-                        tc_commit(bar(B_TF + 2 * w + b));
+                        tc_commit(bar(B_TF + kBufs * w + b));
                     }
                     tc_commit(bar(B_SE + s));
                 }
@@ -274,37 +284,43 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
             if (2 * pr + w >= g) break;
             const int hq = h * g + 2 * pr + w;
             const float c2 = kFp8 ? a.scale_log2 * __ldg(a.q_scale + hq) : a.scale_log2;
-            if constexpr (kFp8) {
-                // this head's 128 query rows -> bf16 (exact), 128-byte swizzled K-major tile
+            {
+                // this head's query rows -> TMEM as the MMA's A operand (e4m3 codes
+                // are converted exactly to bf16); 32 columns = 64 values at a time
                 if (pr >= 1) {
                     const bool got = mbar_wait(bar(B_QE + w), (pr - 1) & 1, abort_flag, a.status, a.wait_ns);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 }
-                uint8_t *qt = smem + kSmQ + w * kQBytes;
                 const int qi = il * kBlock + rowt;
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    a.q8 + (long long)(rq.q_off + qi) * a.q_stride_tok + (long long)hq * a.q_stride_head);
+                const long long el = (long long)(rq.q_off + qi) * a.q_stride_tok + (long long)hq * a.q_stride_head;
 #pragma unroll
-                for (int v = 0; v < 8; ++v) {                      // 16 codes per 16-byte load
-                    const uint4 c16 = row_valid ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-                    const uint32_t cw[4] = {c16.x, c16.y, c16.z, c16.w};
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t qw[32];
+                    if constexpr (!kFp8) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(a.q16 + el) + half * 8;
 #pragma unroll
-                    for (int half8 = 0; half8 < 2; ++half8) {      // 8 codes -> one 16-byte bf16 chunk
-                        uint32_t o[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint32_t word = cw[half8 * 2 + k / 2];
-                            const __nv_fp8x2_storage_t c2v = (__nv_fp8x2_storage_t)(word >> (16 * (k & 1)));
-                            const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(c2v, __NV_E4M3)));
-                            o[k] = pack_bf16x2(f.x, f.y);
+                        for (int v = 0; v < 8; ++v) {
+                            const uint4 c = row_valid ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                            qw[4 * v] = c.x; qw[4 * v + 1] = c.y; qw[4 * v + 2] = c.z; qw[4 * v + 3] = c.w;
                         }
-                        const int col = v * 16 + half8 * 8;           // first of the 8 columns
-                        const int hf = col >> 6, j = (col & 63) >> 3;
-                        *reinterpret_cast<uint4 *>(qt + hf * (kQBytes / 2) + rowt * 128 + ((j ^ (rowt & 7)) << 4)) =
-                            make_uint4(o[0], o[1], o[2], o[3]);
+                    } else {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(a.q8 + el) + half * 4;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const uint4 c = row_valid ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                            const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                const __nv_fp8x2_storage_t c2v = (__nv_fp8x2_storage_t)(cw[k / 2] >> (16 * (k & 1)));
+                                const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(c2v, __NV_E4M3)));
+                                qw[8 * v + k] = pack_bf16x2(f.x, f.y);
+                            }
+                        }
                     }
+                    tmem_st32(lane_base + kTmemQ + w * 64 + half * 32, qw);
                 }
-                fence_proxy_async();                               // visible to the tensor core
+                tmem_st_wait();
+                tc_fence_before();
                 mbar_arrive(bar(B_QF + w));
             }
             float m = -INFINITY;
@@ -312,40 +328,40 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
             for (int pass = 0; pass < 2 && ok; ++pass) {
                 if (pass == 1) mc2 = (m == -INFINITY || !row_valid) ? 0.f : m * c2;
                 for (int c = 0; c < nch; ++c, ++u) {
-                    const int b = u & 1;
-                    const bool got = mbar_wait(bar(B_TF + 2 * w + b), (u >> 1) & 1, abort_flag, a.status, a.wait_ns);
+                    const int b = u % kBufs;
+                    const bool got = mbar_wait(bar(B_TF + kBufs * w + b), (u / kBufs) & 1, abort_flag, a.status,
+                                               a.wait_ns);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     tc_fence_after();
-                    uint32_t u0[32], u1[32];
-                    tmem_ld32(lane_base + (2 * w + b) * kChunk, u0);
-                    tmem_ld32(lane_base + (2 * w + b) * kChunk + 32, u1);
-                    tmem_ld_wait();
-                    reg_fence(u0);
-                    reg_fence(u1);
-                    tc_fence_before();
-                    mbar_arrive(bar(B_TE + 2 * w + b));
-                    const int J0 = c * kChunk;
-                    if (pass == 0) {
-                        float m4[4] = {m, -INFINITY, -INFINITY, -INFINITY};
+                    const uint32_t colb = lane_base + (kBufs * w + b) * kChunk;
+                    float m4[4] = {m, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            if (J0 + e < ncol) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(u0[e]));
-                            if (J0 + 32 + e < ncol) m4[(e + 2) & 3] = fmaxf(m4[(e + 2) & 3], __uint_as_float(u1[e]));
+                    for (int sl = 0; sl < kChunk / 32; ++sl) {
+                        uint32_t u0[32];
+                        tmem_ld32(colb + sl * 32, u0);
+                        tmem_ld_wait();
+                        reg_fence(u0);
+                        if (sl == kChunk / 32 - 1) {           // the buffer is free once read
+                            tc_fence_before();
+                            mbar_arrive(bar(B_TE + kBufs * w + b));
                         }
-                        m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                    } else {
-                        float v0[32], v1[32];
+                        const int J0 = c * kChunk + sl * 32;
+                        if (pass == 0) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            v0[e] = (row_valid && J0 + e < ncol) ? fast_exp2(fmaf(__uint_as_float(u0[e]), c2, -mc2)) : 0.f;
-                            v1[e] = (row_valid && J0 + 32 + e < ncol) ? fast_exp2(fmaf(__uint_as_float(u1[e]), c2, -mc2)) : 0.f;
+                            for (int e = 0; e < 32; ++e)
+                                if (J0 + e < ncol) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(u0[e]));
+                        } else {
+                            float v0[32];
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                v0[e] = (row_valid && J0 + e < ncol) ? fast_exp2(fmaf(__uint_as_float(u0[e]), c2, -mc2))
+                                                                      : 0.f;
+                            // lane L now gets the sum of column J0 + L over this warp's 32 rows
+                            const float s0 = transpose_reduce32(v0, lane);
+                            if (J0 + lane < ncol) my_acc[J0 + lane] += s0;
                         }
-                        const float s0 = transpose_reduce32(v0, lane);
-                        const float s1 = transpose_reduce32(v1, lane);
-                        // lane L now holds the sums of columns J0 + L and J0 + 32 + L
-                        if (J0 + lane < ncol) my_acc[J0 + lane] += s0;
-                        if (J0 + 32 + lane < ncol) my_acc[J0 + 32 + lane] += s1;
                     }
+                    if (pass == 0) m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 }
             }
         }
@@ -380,7 +396,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -432,9 +448,14 @@ bool map3(CUtensorMap *m, const void *base, long long n1, long long n2, long lon
 
 }  // namespace
 
-int score_tc_rows_pad(const BatchDesc &bd) { return bd.total_kb > kChunk ? bd.total_kb : kChunk; }
+// rows of each mean term: at least one box of the widest chunk
+int score_tc_rows_pad(const BatchDesc &bd) { return bd.total_kb > 128 ? bd.total_kb : 128; }
 
-size_t score_tc_smem_bytes(int max_nkb) { return (size_t)kSmAcc + 8 * sizeof(float) * max_nkb + 1024; }
+// shared memory of the build that serves rows of up to max_nkb blocks
+size_t score_tc_smem_bytes(int max_nkb) {
+    const size_t wide = ScoreCfg<128>::smem_bytes(max_nkb);
+    return wide <= 227 * 1024 ? wide : ScoreCfg<64>::smem_bytes(max_nkb);
+}
 
 cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
                             long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
@@ -447,12 +468,14 @@ cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long l
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap tmQ, tmM;
-    if (!fp8 && !map3(&tmQ, q, bd.h_q, bd.total_q, q_stride_head, q_stride_tok, kBlock)) return cudaErrorInvalidValue;
-    if (!map3(&tmM, terms, bd.h_kv, 3LL * rows_pad, kHeadDim, (long long)bd.h_kv * kHeadDim, kChunk))
+    (void)q_stride_head;
+    const bool wide = ScoreCfg<128>::smem_bytes(bd.max_nkb) <= 227 * 1024;
+    if (!map3(&tmM, terms, bd.h_kv, 3LL * rows_pad, kHeadDim, (long long)bd.h_kv * kHeadDim, wide ? 128 : 64))
         return cudaErrorInvalidValue;
     ScoreTcArgs a;
     a.score = score;
     a.q8 = (const uint8_t *)q;
+    a.q16 = (const __nv_bfloat16 *)q;
     a.q_stride_tok = q_stride_tok;
     a.q_stride_head = q_stride_head;
     a.q_scale = q_scale;
@@ -461,9 +484,10 @@ cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long l
     a.acc_stride = bd.max_nkb;
     a.status = status;
     a.wait_ns = wait_ns;
-    if (fp8) tmQ = tmM;                  // not read: the row warps load e4m3 queries themselves
+    tmQ = tmM;                           // not read: the row warps load the queries themselves
     const int smem = (int)score_tc_smem_bytes(bd.max_nkb);
-    auto kern = fp8 ? score_tc_kernel<true> : score_tc_kernel<false>;
+    auto kern = wide ? (fp8 ? score_tc_kernel<true, 128> : score_tc_kernel<false, 128>)
+                     : (fp8 ? score_tc_kernel<true, 64> : score_tc_kernel<false, 64>);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<bd.total_rows, kScThreads, smem, st>>>(bd, tmQ, tmM, a);

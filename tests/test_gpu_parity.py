@@ -202,18 +202,19 @@ def test_fp8_attention_sharp_varlen(mean_corr):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
-def test_rows_longer_than_2048_blocks_use_the_fp32_score_kernel(dtype):
-    """A 262,272-token request (2049 key blocks) is past the tensor-core score
-    kernel's shared-memory limit: its scores come from the fp32 CUDA-core
-    kernel.  Sampled score rows and their index rows against the oracle."""
+def test_rows_past_the_tensor_core_limit_use_the_fp32_score_kernel(dtype):
+    """A 345,600-token request (2700 key blocks) is past the tensor-core score
+    kernel's shared-memory limit (2647 blocks for its 64-block chunks): its
+    scores come from the fp32 CUDA-core kernel.  Sampled score rows and their
+    index rows against the oracle."""
     import oracle
     import torch
     from block_sparse_long_fp_gb300 import fprefill
-    L = 2049 * 128
+    L = 2700 * 128
     spec = synth.Spec("long-rows", [(L, 0)], 2, 1, page_size=128, layout="shuffled", dtype=dtype,
                       n_needles=2, logit_scale=4.0, config_id=77)
     case = synth.make_case(spec)
-    rows = np.array([0, 5, 700, 2047, 2048])
+    rows = np.array([0, 5, 700, 2048, 2699])
     ref = oracle.discover_and_select(case, row_subset=lambda r, nqb, hkv: rows)
     layer = fprefill.layer_from_case(case)
     k_mean, v_mean, score = layer.discover()
