@@ -105,7 +105,8 @@ bool use_score_tc(const fp_problem *p, const BatchDesc &bd) {
 
 size_t attn_ws_bytes(const BatchDesc &bd) {
     size_t n = kWsHeaderBytes;
-    n += align_up((size_t)bd.total_rows * (bd.g / 2 > 0 ? bd.g / 2 : 1) * sizeof(int), 256);
+    // work schedule and, after it, the work-list cursor
+    n += align_up(((size_t)bd.total_rows * (bd.g / 2 > 0 ? bd.g / 2 : 1) + 1) * sizeof(int), 256);
     n += 2 * align_up((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2, 256);
     return n;
 }
@@ -246,7 +247,7 @@ static fp_status run_attn(const fp_problem *p, const fp_params *prm, const int *
     L.status = status_ptr(ws);
     size_t off = kWsHeaderBytes;
     L.work = reinterpret_cast<int *>(w + off);
-    off += align_up((size_t)bd.total_rows * (bd.g / 2) * sizeof(int), 256);
+    off += align_up(((size_t)bd.total_rows * (bd.g / 2 > 0 ? bd.g / 2 : 1) + 1) * sizeof(int), 256);
     L.km16 = reinterpret_cast<__nv_bfloat16 *>(w + off);
     off += align_up((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2, 256);
     L.vm16 = reinterpret_cast<__nv_bfloat16 *>(w + off);

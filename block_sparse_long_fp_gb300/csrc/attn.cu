@@ -10,8 +10,11 @@
 // for the group (PackGQA, V2 section 4.2 (1)).
 //
 // How (sm_103a design, not the Hopper one of the pages):
-//  * one CTA = one work unit = (index row (request, query block I, kv head h),
-//    a pair of query heads of the group): two 128-query tiles Q0, Q1;
+//  * a work unit = (index row (request, query block I, kv head h), a pair of
+//    query heads of the group): two 128-query tiles Q0, Q1;
+//  * persistent CTAs, one per SM, take units off a list sorted by decreasing
+//    work; warp 2 prepares the next unit's metadata (kept-block bitmap, mean
+//    tiles) while the current one runs;
 //  * warp 0 issues TMA loads (Q once; K and V tiles through the page table
 //    into a two-stage ring each; mean tiles from the bf16 copies of the block
 //    means);
@@ -39,7 +42,7 @@ namespace fp {
 
 using namespace sm100;
 
-constexpr int kAttnThreads = 384;     // 3 warpgroups: control (TMA, MMA), softmax tile 0, tile 1
+constexpr int kAttnThreads = 384;     // 3 warpgroups: control (TMA, MMA, unit metadata), softmax tile 0, tile 1
 // register split (setmaxnreg): the launch grants 168 per thread; the control
 // warpgroup gives some back so the softmax warpgroups can hold a whole
 // 128-column row of S: 104*128 + 2*192*128 <= 168*384.
@@ -54,15 +57,35 @@ constexpr int kSmemV = 4 * kTileBytes;
 constexpr int kSmemCtl = 6 * kTileBytes;                   // 192 KB
 constexpr int kBitmapWords = FP_MAX_KEY_BLOCKS / 32;
 constexpr int kMaxCorrTiles = FP_MAX_KEY_BLOCKS / kBlock;
-constexpr int kSmemAttn = kSmemCtl + 256 + kBitmapWords * 4 + kMaxCorrTiles * 4 + 1024;
 
-enum { BAR_Q = 0, BAR_KF = 1, BAR_KE = 3, BAR_VF = 5, BAR_VE = 7, BAR_SF = 9, BAR_PF = 11, BAR_OF = 13,
-       NUM_BARS = 15 };
+enum { BAR_Q = 0, BAR_QE = 1, BAR_KF = 2, BAR_KE = 4, BAR_VF = 6, BAR_VE = 8, BAR_SF = 10, BAR_PF = 12,
+       BAR_OF = 14, BAR_MF = 16, BAR_ME = 18, NUM_BARS = 20 };
+// arrivals on a metadata-empty barrier: the TMA thread, the MMA thread and
+// one lane of each of the eight softmax warps
+constexpr int kMetaConsumers = 10;
+
+// What the metadata warp prepares for one unit, double-buffered so that it
+// runs one unit ahead of the others.
+struct UnitMeta {
+    int pos;                          // position in the work list; -1: no more units
+    int unit;                         // unit id
+    int n_items;                      // kept blocks + mean tiles
+    int n_corr;                       // mean tiles
+    uint32_t bitmap[kBitmapWords];    // kept blocks J < I
+    int corr[kMaxCorrTiles];          // mean tiles holding a skipped block
+};
+constexpr int kSmemMisc = kSmemCtl + NUM_BARS * 8;         // TMEM address, abort flag
+constexpr int kSmemMeta = kSmemCtl + 256;
+constexpr int kSmemAttn = kSmemMeta + 2 * (int)sizeof(UnitMeta) + 1024;
+static_assert(NUM_BARS * 8 + 8 <= 256, "control block");
+static_assert(sizeof(UnitMeta) % 16 == 0, "metadata buffers");
 
 struct AttnArgs {
     const int *row_ptr;       // null in dense mode
     const int *col_idx;
     const int *work;          // unit ids sorted by decreasing work
+    int *next_unit;           // work-list cursor (zeroed by the schedule kernel)
+    int n_units;
     const int *block_table;
     int max_pages;
     int page_size;
@@ -85,10 +108,39 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// one work unit: index row (request r, query block I, kv head h) and a pair of
+// query heads hq0, hq0 + 1 of the group
+struct Unit {
+    int row, r, il, h, I, hq0, rp0, n_kept;
+};
+
+__device__ __forceinline__ Unit decode_unit(const BatchDesc &bd, const AttnArgs &a, int unit) {
+    Unit U;
+    U.row = unit / a.n_pairs;
+    const int pair = unit % a.n_pairs;
+    U.r = req_of_row(bd, U.row);
+    const ReqDesc &rq = bd.req[U.r];
+    const int local = U.row - rq.row_base;
+    U.il = local / bd.h_kv;
+    U.h = local % bd.h_kv;
+    U.I = rq.start / kBlock + U.il;
+    U.hq0 = U.h * bd.g + 2 * pair;
+    U.rp0 = a.row_ptr ? __ldg(a.row_ptr + U.row) : 0;
+    U.n_kept = a.row_ptr ? __ldg(a.row_ptr + U.row + 1) - U.rp0 : U.I + 1;
+    return U;
+}
+
 // kFp8: q, k, v (and the block-mean tiles) are e4m3 codes with per-head
 // scales; both MMAs run as kind::f8f6f4 and P is stored in TMEM as e4m3 of
 // 256 * p (the scaling of the V2 paper reading, section 4.2 (4), which keeps
 // the weights in e4m3's normal range; it cancels in the ratio).
+//
+// Persistent: one CTA per SM walks the work list (a shared cursor, so the
+// longest units go first and each SM takes the next unit when it is ready).
+// Barrier phases run on counters that span units: `it` counts the CTA's
+// items (K/V ring slots, S and P handshakes), `kq` its non-empty units (Q and
+// O handshakes), `k` all its units (metadata buffers).  The next unit's Q,
+// K and V loads and its first S MMAs overlap the current unit's epilogue.
 template <bool kFp8>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtensorMap tmQ,
@@ -98,11 +150,9 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmemCtl);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kSmemCtl + NUM_BARS * 8);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kSmemCtl + NUM_BARS * 8 + 4);
-    int *n_corr_s = reinterpret_cast<int *>(smem + kSmemCtl + NUM_BARS * 8 + 8);
-    uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem + kSmemCtl + 256);
-    int *corr_list = reinterpret_cast<int *>(smem + kSmemCtl + 256 + kBitmapWords * 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kSmemMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kSmemMisc + 4);
+    UnitMeta *meta = reinterpret_cast<UnitMeta *>(smem + kSmemMeta);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t sbase = smem_u32(smem);
@@ -111,62 +161,20 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
     // e4m3 in one 128-column box; smem slots are 32 KB either way
     constexpr int kT = kFp8 ? kTileBytes / 2 : kTileBytes;
     constexpr int kNH = kFp8 ? 1 : 2;
-
-    // ---- the unit ------------------------------------------------------------
-    const int unit = a.work[blockIdx.x];
-    const int row = unit / a.n_pairs;
-    const int pair = unit % a.n_pairs;
-    const int r = req_of_row(bd, row);
-    const ReqDesc &rq = bd.req[r];
-    const int local = row - rq.row_base;
-    const int il = local / bd.h_kv;
-    const int h = local % bd.h_kv;
-    const int I = rq.start / kBlock + il;
-    const int hq0 = h * bd.g + 2 * pair;
     const bool sparse = a.row_ptr != nullptr;
-    const int rp0 = sparse ? a.row_ptr[row] : 0;
-    const int n_kept = sparse ? a.row_ptr[row + 1] - rp0 : I + 1;
 
-    // ---- set-up ----------------------------------------------------------------
+    // ---- set-up (once per CTA) ---------------------------------------------------
     if (threadIdx.x == 0) {
         for (int k = 0; k < NUM_BARS; ++k) {
-            uint32_t cnt = (k == BAR_PF || k == BAR_PF + 1) ? 128u : 1u;
+            uint32_t cnt = 1u;
+            if (k == BAR_PF || k == BAR_PF + 1) cnt = 128u;
+            if (k == BAR_MF || k == BAR_MF + 1) cnt = 32u;
+            if (k == BAR_ME || k == BAR_ME + 1) cnt = kMetaConsumers;
             mbar_init(bar(k), cnt);
         }
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async();
-    }
-    if (warp == 0) {
-        // kept-block bitmap and the list of mean tiles holding a skipped block
-        int n_corr = 0;
-        if (sparse && a.mean_corr && I > 0) {
-            const int nw = (I + 31) / 32;
-            for (int w = lane; w < nw; w += 32) bitmap[w] = 0u;
-            __syncwarp();
-            for (int k = lane; k < n_kept; k += 32) {
-                int J = __ldg(a.col_idx + rp0 + k);
-                if (J >= 0 && J < I) atomicOr(&bitmap[J >> 5], 1u << (J & 31));
-            }
-            __syncwarp();
-            const int ntiles = (I + kBlock - 1) / kBlock;
-            for (int c0 = 0; c0 < ntiles; c0 += 32) {
-                int c = c0 + lane;
-                bool any = false;
-                if (c < ntiles) {
-                    for (int w = 0; w < 4; ++w) {
-                        int J0 = c * kBlock + w * 32;
-                        if (J0 >= I) break;
-                        uint32_t valid = (I - J0 >= 32) ? 0xffffffffu : ((1u << (I - J0)) - 1u);
-                        if (~bitmap[J0 >> 5] & valid) any = true;
-                    }
-                }
-                unsigned m = __ballot_sync(0xffffffffu, any);
-                if (any) corr_list[n_corr + __popc(m & ((1u << lane) - 1u))] = c;
-                n_corr += __popc(m);
-            }
-        }
-        if (lane == 0) *n_corr_s = n_corr;
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), 512);
@@ -176,7 +184,6 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int n_items = n_kept + *n_corr_s;
     // a CTA of this launch (or an earlier one on this workspace) timed out:
     // do no work, so a broken launch ends in one wait limit, not one per CTA
     const bool dead = a.status && *reinterpret_cast<volatile int *>(a.status) == FP_ERR_TIMEOUT;
@@ -184,113 +191,209 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
     // each role's code sits under its own register budget
     if (warp < 4) {
         setmaxnreg_dec<kRegsControl>();
-        if (!dead && n_items > 0 && warp == 0) {
-            // ================= TMA producer =================
-            if (lane == 0) {
-                tma_prefetch_desc(&tmQ);
-                tma_prefetch_desc(&tmK);
-                tma_prefetch_desc(&tmV);
-                const int q_row0 = rq.q_off + il * kBlock;
-                mbar_expect_tx(bar(BAR_Q), 2 * kT);
-                for (int t = 0; t < 2; ++t)
-                    for (int hf = 0; hf < kNH; ++hf)
-                        tma_load_3d(sbase + kSmemQ + t * kTileBytes + hf * kHalfBytes, &tmQ, bar(BAR_Q),
-                                    hf * 64, hq0 + t, q_row0);
-                const int rpb = a.page_size < kBlock ? a.page_size : kBlock;   // rows per box
-                const int oob = a.num_pages * a.page_size;                     // zero-filled rows
-                const int *bt = a.block_table + (long long)r * a.max_pages;
-                const int npages_req = (rq.lk + a.page_size - 1) / a.page_size;
-                for (int j = 0; j < n_items; ++j) {
-                    const int s = j & 1, ph = (j >> 1) & 1;
-                    const bool kept = j < n_kept;
-                    int J = 0, c = 0;
-                    if (kept) J = sparse ? __ldg(a.col_idx + rp0 + j) : j;
-                    else c = corr_list[j - n_kept];
-                    for (int op = 0; op < 2; ++op) {       // 0: K tile, 1: V tile
-                        const uint32_t full = bar(op == 0 ? BAR_KF + s : BAR_VF + s);
-                        if (j >= 2 && !mbar_wait(bar(op == 0 ? BAR_KE + s : BAR_VE + s), ph ^ 1, abort_flag,
-                                                 a.status, a.wait_ns))
-                            goto producer_done;
-                        const uint32_t dst = sbase + (op == 0 ? kSmemK : kSmemV) + s * kTileBytes;
-                        mbar_expect_tx(full, kT);
-                        if (kept) {
-                            const CUtensorMap *tm = op == 0 ? &tmK : &tmV;
-                            for (int sub = 0; sub < kBlock / rpb; ++sub) {
-                                const int tok = J * kBlock + sub * rpb;
-                                int z = oob;
-                                const int lp = tok / a.page_size;
-                                if (tok < rq.lk && lp < npages_req) {
-                                    const int pg = __ldg(bt + lp);
-                                    if (pg >= 0 && pg < a.num_pages) z = pg * a.page_size + tok % a.page_size;
-                                    else set_status(a.status, FP_ERR_DEVICE_BOUNDS);
+        if (dead) {
+        } else if (warp == 2) {
+            // ================= unit metadata =================
+            // takes the next unit off the work list, builds its kept-block
+            // bitmap and the list of mean tiles holding a skipped block
+            for (int k = 0;; ++k) {
+                const int b = k & 1;
+                UnitMeta &M = meta[b];
+                if (k >= 2) {
+                    const bool got = mbar_wait(bar(BAR_ME + b), ((k >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_ns);
+                    if (!__all_sync(0xffffffffu, got)) break;
+                }
+                int pos = 0;
+                if (lane == 0) pos = atomicAdd(a.next_unit, 1);
+                pos = __shfl_sync(0xffffffffu, pos, 0);
+                const bool end = pos >= a.n_units;
+                int unit = 0, n_corr = 0, n_kept = 0;
+                if (!end) {
+                    unit = __ldg(a.work + pos);
+                    const Unit U = decode_unit(bd, a, unit);
+                    n_kept = U.n_kept;
+                    const int I = U.I;
+                    if (sparse && a.mean_corr && I > 0) {
+                        const int nw = (I + 31) / 32;
+                        for (int w = lane; w < nw; w += 32) M.bitmap[w] = 0u;
+                        __syncwarp();
+                        for (int j = lane; j < U.n_kept; j += 32) {
+                            const int J = __ldg(a.col_idx + U.rp0 + j);
+                            if (J >= 0 && J < I) atomicOr(&M.bitmap[J >> 5], 1u << (J & 31));
+                        }
+                        __syncwarp();
+                        const int ntiles = (I + kBlock - 1) / kBlock;
+                        for (int c0 = 0; c0 < ntiles; c0 += 32) {
+                            const int c = c0 + lane;
+                            bool any = false;
+                            if (c < ntiles) {
+                                for (int w = 0; w < 4; ++w) {
+                                    const int J0 = c * kBlock + w * 32;
+                                    if (J0 >= I) break;
+                                    const uint32_t valid = (I - J0 >= 32) ? 0xffffffffu : ((1u << (I - J0)) - 1u);
+                                    if (~M.bitmap[J0 >> 5] & valid) any = true;
                                 }
-                                for (int hf = 0; hf < kNH; ++hf)
-                                    tma_load_3d(dst + hf * kHalfBytes + sub * rpb * 128, tm, full, hf * 64, h, z);
                             }
-                        } else {
-                            const CUtensorMap *tm = op == 0 ? &tmKm : &tmVm;
-                            for (int hf = 0; hf < kNH; ++hf)
-                                tma_load_3d(dst + hf * kHalfBytes, tm, full, hf * 64, h, rq.kb_base + c * kBlock);
+                            const unsigned m = __ballot_sync(0xffffffffu, any);
+                            if (any) M.corr[n_corr + __popc(m & ((1u << lane) - 1u))] = c;
+                            n_corr += __popc(m);
                         }
                     }
                 }
-            producer_done:;
+                if (lane == 0) {
+                    M.pos = end ? -1 : pos;
+                    M.unit = unit;
+                    M.n_items = n_kept + n_corr;
+                    M.n_corr = n_corr;
+                }
+                __syncwarp();
+                mbar_arrive(bar(BAR_MF + b));
+                if (end) break;
             }
-        } else if (!dead && n_items > 0 && warp == 1) {
+        } else if (warp == 0 && lane == 0) {
+            // ================= TMA producer =================
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            const int rpb = a.page_size < kBlock ? a.page_size : kBlock;   // rows per box
+            const int oob = a.num_pages * a.page_size;                     // zero-filled rows
+            uint32_t it = 0;
+            int kq = 0;
+            for (int k = 0;; ++k) {
+                const int b = k & 1;
+                const UnitMeta &M = meta[b];
+                if (!mbar_wait(bar(BAR_MF + b), (k >> 1) & 1, abort_flag, a.status, a.wait_ns)) break;
+                if (M.pos < 0) break;
+                const int n_items = M.n_items;
+                if (n_items > 0) {
+                    const Unit U = decode_unit(bd, a, M.unit);
+                    const ReqDesc &rq = bd.req[U.r];
+                    // Q of the previous unit is free once its last S MMAs are done
+                    if (kq > 0 && !mbar_wait(bar(BAR_QE), (kq - 1) & 1, abort_flag, a.status, a.wait_ns)) break;
+                    const int q_row0 = rq.q_off + U.il * kBlock;
+                    mbar_expect_tx(bar(BAR_Q), 2 * kT);
+                    for (int t = 0; t < 2; ++t)
+                        for (int hf = 0; hf < kNH; ++hf)
+                            tma_load_3d(sbase + kSmemQ + t * kTileBytes + hf * kHalfBytes, &tmQ, bar(BAR_Q),
+                                        hf * 64, U.hq0 + t, q_row0);
+                    const int *bt = a.block_table + (long long)U.r * a.max_pages;
+                    const int npages_req = (rq.lk + a.page_size - 1) / a.page_size;
+                    bool good = true;
+                    for (int j = 0; j < n_items && good; ++j, ++it) {
+                        const int s = it & 1, ph = (it >> 1) & 1;
+                        const bool kept = j < U.n_kept;
+                        int J = 0, c = 0;
+                        if (kept) J = sparse ? __ldg(a.col_idx + U.rp0 + j) : j;
+                        else c = M.corr[j - U.n_kept];
+                        for (int op = 0; op < 2; ++op) {       // 0: K tile, 1: V tile
+                            const uint32_t full = bar(op == 0 ? BAR_KF + s : BAR_VF + s);
+                            if (it >= 2 && !mbar_wait(bar(op == 0 ? BAR_KE + s : BAR_VE + s), ph ^ 1, abort_flag,
+                                                      a.status, a.wait_ns)) {
+                                good = false;
+                                break;
+                            }
+                            const uint32_t dst = sbase + (op == 0 ? kSmemK : kSmemV) + s * kTileBytes;
+                            mbar_expect_tx(full, kT);
+                            if (kept) {
+                                const CUtensorMap *tm = op == 0 ? &tmK : &tmV;
+                                for (int sub = 0; sub < kBlock / rpb; ++sub) {
+                                    const int tok = J * kBlock + sub * rpb;
+                                    int z = oob;
+                                    const int lp = tok / a.page_size;
+                                    if (tok < rq.lk && lp < npages_req) {
+                                        const int pg = __ldg(bt + lp);
+                                        if (pg >= 0 && pg < a.num_pages) z = pg * a.page_size + tok % a.page_size;
+                                        else set_status(a.status, FP_ERR_DEVICE_BOUNDS);
+                                    }
+                                    for (int hf = 0; hf < kNH; ++hf)
+                                        tma_load_3d(dst + hf * kHalfBytes + sub * rpb * 128, tm, full, hf * 64, U.h, z);
+                                }
+                            } else {
+                                const CUtensorMap *tm = op == 0 ? &tmKm : &tmVm;
+                                for (int hf = 0; hf < kNH; ++hf)
+                                    tma_load_3d(dst + hf * kHalfBytes, tm, full, hf * 64, U.h, rq.kb_base + c * kBlock);
+                            }
+                        }
+                    }
+                    if (!good) break;
+                    ++kq;
+                }
+                mbar_arrive(bar(BAR_ME + b));
+            }
+        } else if (warp == 1 && lane == 0) {
             // ================= MMA issuer =================
-            if (lane == 0) {
-                constexpr uint32_t idS = kFp8 ? idesc_e4m3(128, 128, false) : idesc_bf16(128, 128, false);
-                constexpr uint32_t idPV = kFp8 ? idesc_e4m3(128, 128, true) : idesc_bf16(128, 128, true);
-                constexpr int kKSteps = kFp8 ? 4 : 8;                // K = 32 (e4m3) or 16 (bf16) per MMA
-                constexpr int kKeysPerStep = kFp8 ? 32 : 16;
-                // descriptors differ only in the start address: add offsets (in 16-byte units)
-                const uint64_t qdesc = smem_desc_sw128(sbase + kSmemQ, 16, 1024);
-                const uint64_t kdesc = smem_desc_sw128(sbase + kSmemK, 16, 1024);
-                const uint64_t vdesc = smem_desc_sw128(sbase + kSmemV, kFp8 ? 16 : kHalfBytes, 1024);
-                auto issue_S = [&](int t, int s) {
-                    const uint64_t qd = qdesc + ((t * kTileBytes) >> 4);
-                    const uint64_t kd = kdesc + ((s * kTileBytes) >> 4);
+            constexpr uint32_t idS = kFp8 ? idesc_e4m3(128, 128, false) : idesc_bf16(128, 128, false);
+            constexpr uint32_t idPV = kFp8 ? idesc_e4m3(128, 128, true) : idesc_bf16(128, 128, true);
+            constexpr int kKSteps = kFp8 ? 4 : 8;                // K = 32 (e4m3) or 16 (bf16) per MMA
+            constexpr int kKeysPerStep = kFp8 ? 32 : 16;
+            // descriptors differ only in the start address: add offsets (in 16-byte units)
+            const uint64_t qdesc = smem_desc_sw128(sbase + kSmemQ, 16, 1024);
+            const uint64_t kdesc = smem_desc_sw128(sbase + kSmemK, 16, 1024);
+            const uint64_t vdesc = smem_desc_sw128(sbase + kSmemV, kFp8 ? 16 : kHalfBytes, 1024);
+            auto issue_S = [&](int t, int s) {
+                const uint64_t qd = qdesc + ((t * kTileBytes) >> 4);
+                const uint64_t kd = kdesc + ((s * kTileBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kKSteps; ++kk) {
-                        const uint32_t off = (kFp8 ? kk * 32 : (kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-                        if constexpr (kFp8) mma_ss_f8(tmem + t * 256, qd + off, kd + off, idS, kk > 0);
-                        else mma_ss(tmem + t * 256, qd + off, kd + off, idS, kk > 0);
-                    }
-                };
-                auto issue_PV = [&](int t, int s, bool acc) {
-                    const uint64_t vd = vdesc + ((s * kTileBytes) >> 4);
+                for (int kk = 0; kk < kKSteps; ++kk) {
+                    const uint32_t off = (kFp8 ? kk * 32 : (kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                    if constexpr (kFp8) mma_ss_f8(tmem + t * 256, qd + off, kd + off, idS, kk > 0);
+                    else mma_ss(tmem + t * 256, qd + off, kd + off, idS, kk > 0);
+                }
+            };
+            auto issue_PV = [&](int t, int s, bool acc) {
+                const uint64_t vd = vdesc + ((s * kTileBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kKSteps; ++kk) {
-                        const uint64_t b = vd + ((kk * kKeysPerStep * 128) >> 4);
-                        if constexpr (kFp8) mma_ts_f8(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, b, idPV, (acc || kk > 0));
-                        else mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, b, idPV, (acc || kk > 0));
-                    }
-                };
-                if (!mbar_wait(bar(BAR_Q), 0, abort_flag, a.status, a.wait_ns)) goto mma_done;
-                if (!mbar_wait(bar(BAR_KF), 0, abort_flag, a.status, a.wait_ns)) goto mma_done;
+                for (int kk = 0; kk < kKSteps; ++kk) {
+                    const uint64_t b = vd + ((kk * kKeysPerStep * 128) >> 4);
+                    if constexpr (kFp8) mma_ts_f8(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, b, idPV, (acc || kk > 0));
+                    else mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, b, idPV, (acc || kk > 0));
+                }
+            };
+            uint32_t it = 0;
+            int kq = 0;
+            for (int k = 0;; ++k) {
+                const int b = k & 1;
+                if (!mbar_wait(bar(BAR_MF + b), (k >> 1) & 1, abort_flag, a.status, a.wait_ns)) break;
+                const int pos = meta[b].pos, n_items = meta[b].n_items;
+                mbar_arrive(bar(BAR_ME + b));
+                if (pos < 0) break;
+                if (n_items == 0) continue;
+                if (!mbar_wait(bar(BAR_Q), kq & 1, abort_flag, a.status, a.wait_ns)) break;
+                if (!mbar_wait(bar(BAR_KF + (it & 1)), (it >> 1) & 1, abort_flag, a.status, a.wait_ns)) break;
                 tc_fence_after();
-                issue_S(0, 0);
+                issue_S(0, it & 1);
                 tc_commit(bar(BAR_SF + 0));
-                issue_S(1, 0);
+                issue_S(1, it & 1);
                 tc_commit(bar(BAR_SF + 1));
-                tc_commit(bar(BAR_KE + 0));
-                for (int j = 0; j < n_items; ++j) {
-                    const int s = j & 1, ph = (j >> 1) & 1;
-                    const int s1 = (j + 1) & 1, ph1 = ((j + 1) >> 1) & 1;
+                tc_commit(bar(BAR_KE + (it & 1)));
+                if (n_items == 1) tc_commit(bar(BAR_QE));
+                bool good = true;
+                for (int j = 0; j < n_items; ++j, ++it) {
+                    const int s = it & 1, ph = (it >> 1) & 1;
+                    const int s1 = (it + 1) & 1, ph1 = ((it + 1) >> 1) & 1;
                     const bool more = j + 1 < n_items;
-                    if (!mbar_wait(bar(BAR_VF + s), ph, abort_flag, a.status, a.wait_ns)) goto mma_done;
-                    if (!mbar_wait(bar(BAR_PF + 0), j & 1, abort_flag, a.status, a.wait_ns)) goto mma_done;
+                    if (!mbar_wait(bar(BAR_VF + s), ph, abort_flag, a.status, a.wait_ns) ||
+                        !mbar_wait(bar(BAR_PF + 0), it & 1, abort_flag, a.status, a.wait_ns)) {
+                        good = false;
+                        break;
+                    }
                     tc_fence_after();
                     issue_PV(0, s, j > 0);
                     if (more) {
-                        if (!mbar_wait(bar(BAR_KF + s1), ph1, abort_flag, a.status, a.wait_ns)) goto mma_done;
+                        if (!mbar_wait(bar(BAR_KF + s1), ph1, abort_flag, a.status, a.wait_ns)) {
+                            good = false;
+                            break;
+                        }
                         tc_fence_after();
                         issue_S(0, s1);
                         tc_commit(bar(BAR_SF + 0));
                     } else {
                         tc_commit(bar(BAR_OF + 0));
                     }
-                    if (!mbar_wait(bar(BAR_PF + 1), j & 1, abort_flag, a.status, a.wait_ns)) goto mma_done;
+                    if (!mbar_wait(bar(BAR_PF + 1), it & 1, abort_flag, a.status, a.wait_ns)) {
+                        good = false;
+                        break;
+                    }
                     tc_fence_after();
                     issue_PV(1, s, j > 0);
                     tc_commit(bar(BAR_VE + s));
@@ -298,38 +401,62 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         issue_S(1, s1);
                         tc_commit(bar(BAR_SF + 1));
                         tc_commit(bar(BAR_KE + s1));
+                        if (j + 2 == n_items) tc_commit(bar(BAR_QE));   // the unit's last S MMAs
                     } else {
                         tc_commit(bar(BAR_OF + 1));
                     }
                 }
-            mma_done:;
+                if (!good) break;
+                ++kq;
             }
         }
     } else {
         setmaxnreg_inc<kRegsSoftmax>();
-        if (dead) {
-        } else if (n_items > 0) {
-            // ================= softmax warpgroups =================
-            const int t = (warp - 4) / 4;                 // tile
-            const int quarter = warp % 4;                 // TMEM lane quarter of this warp
-            const int rowt = quarter * 32 + lane;         // row of the tile
-            const int qi = il * kBlock + rowt;            // query index inside the request
+        // ================= softmax warpgroups =================
+        const int t = (warp - 4) / 4;                 // tile
+        const int quarter = warp % 4;                 // TMEM lane quarter of this warp
+        const int rowt = quarter * 32 + lane;         // row of the tile
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t tS = lane_base + t * 256;
+        const uint32_t tO = tS + 128;
+        uint32_t it = 0;
+        int kq = 0;
+        for (int k = 0; !dead; ++k) {
+            const int b = k & 1;
+            const UnitMeta &M = meta[b];
+            const bool gotm = mbar_wait(bar(BAR_MF + b), (k >> 1) & 1, abort_flag, a.status, a.wait_ns);
+            if (!__all_sync(0xffffffffu, gotm)) break;
+            if (M.pos < 0) break;
+            const int n_items = M.n_items;
+            const Unit U = decode_unit(bd, a, M.unit);
+            const ReqDesc &rq = bd.req[U.r];
+            const int I = U.I, n_kept = U.n_kept;
+            const int qi = U.il * kBlock + rowt;          // query index inside the request
+            const int head = U.hq0 + t;
+            if (n_items == 0) {
+                // a row with no term at all: O = 0, LSE = -inf
+                if (qi < rq.lq) {
+                    __nv_bfloat16 *dst = a.out + ((long long)(rq.q_off + qi) * bd.h_q + head) * kHeadDim;
+                    for (int c = 0; c < kHeadDim; c += 8) *reinterpret_cast<uint4 *>(dst + c) = make_uint4(0, 0, 0, 0);
+                    if (a.lse) a.lse[(long long)head * bd.total_q + rq.q_off + qi] = -INFINITY;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BAR_ME + b));
+                continue;
+            }
             const int pos = rq.start + qi;                // absolute position
-            const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-            const uint32_t tS = lane_base + t * 256;
-            const uint32_t tO = tS + 128;
             float m = -INFINITY, l = 0.f;
-            const int last_J = n_kept == 0 ? -1 : (sparse ? __ldg(a.col_idx + rp0 + n_kept - 1) : n_kept - 1);
+            const int last_J = n_kept == 0 ? -1 : (sparse ? __ldg(a.col_idx + U.rp0 + n_kept - 1) : n_kept - 1);
             bool ok = true;
             // logit scale (log2 units): e4m3 codes carry the per-head scales
-            const float csc = kFp8 ? a.scale_log2 * __ldg(a.q_scale + hq0 + t) * __ldg(a.k_scale + h) : a.scale_log2;
+            const float csc = kFp8 ? a.scale_log2 * __ldg(a.q_scale + head) * __ldg(a.k_scale + U.h) : a.scale_log2;
             // the running max moves only when it grows by more than kTau (bf16
             // tolerates weights up to 2^8).  For e4m3 it always follows the max, so
             // the largest weight of a row is exactly 256 = e4m3(256 * 1) and only
             // the smaller weights carry e4m3 rounding.
             constexpr float kTau = kFp8 ? 0.f : 8.f;
-            for (int j = 0; j < n_items && ok; ++j) {
-                const bool got = mbar_wait(bar(BAR_SF + t), j & 1, abort_flag, a.status, a.wait_ns);
+            for (int j = 0; j < n_items; ++j, ++it) {
+                const bool got = mbar_wait(bar(BAR_SF + t), it & 1, abort_flag, a.status, a.wait_ns);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }   // tcgen05.ld needs the whole warp
                 tc_fence_after();
                 uint32_t v[4][32];
@@ -359,13 +486,13 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     // mean tile c covers blocks 128c .. 128c+127; a skipped block J < I
                     // is full (only the request's last block can be short, and
                     // it is never before I), so its weight is n_J = 128: bias log2(128)
-                    const int c = corr_list[j - n_kept];
+                    const int c = M.corr[j - n_kept];
                     uint32_t w[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int J0 = c * kBlock + 32 * k;
+                    for (int q = 0; q < 4; ++q) {
+                        const int J0 = c * kBlock + 32 * q;
                         uint32_t valid = J0 >= I ? 0u : (I - J0 >= 32 ? 0xffffffffu : ((1u << (I - J0)) - 1u));
-                        w[k] = valid ? (~bitmap[J0 >> 5] & valid) : 0u;   // 1 = skipped, before I
+                        w[q] = valid ? (~M.bitmap[J0 >> 5] & valid) : 0u;   // 1 = skipped, before I
                     }
 #pragma unroll
                     for (int e = 0; e < 128; ++e)
@@ -375,7 +502,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 // row max: eight independent chains of three-input max, then a tree
                 float mx8[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mx8[k] = x[k];
+                for (int q = 0; q < 8; ++q) mx8[q] = x[q];
 #pragma unroll
                 for (int e = 8; e < 128; e += 2) mx8[(e >> 1) & 7] = max3f(mx8[(e >> 1) & 7], x[e], x[e + 1]);
                 const float mxr = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
@@ -423,7 +550,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     uint32_t pk[32];
                     __half2 hs[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) hs[k] = __float2half2_rn(0.f);
+                    for (int q = 0; q < 4; ++q) hs[q] = __float2half2_rn(0.f);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         float z0, z1, z2, z3;
@@ -459,49 +586,49 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 tc_fence_before();
                 mbar_arrive(bar(BAR_PF + t));
             }
-            // epilogue: O / l -> bf16, LSE
-            const int head = hq0 + t;
-            const bool valid = qi < rq.lq;
-            const bool fin = ok && mbar_wait(bar(BAR_OF + t), 0, abort_flag, a.status, a.wait_ns);
-            if (__all_sync(0xffffffffu, fin)) {
-                tc_fence_after();
-                // O = (sum of weights * v codes) * v_scale / (sum of weights); for e4m3
-                // both sums carry the factor 256, which cancels
-                const float inv = l > 0.f ? (kFp8 ? __ldg(a.v_scale + h) : 1.f) / l : 0.f;
-                __nv_bfloat16 *dst = a.out + ((long long)(rq.q_off + qi) * bd.h_q + head) * kHeadDim;
+            if (!ok) break;
+            // epilogue: O / l -> bf16, LSE.  The unit's fields are decoded again
+            // from the metadata (released only after this) rather than kept live
+            // across the item loop.
+            const Unit V = decode_unit(bd, a, M.unit);
+            const ReqDesc &rv = bd.req[V.r];
+            const int qv = V.il * kBlock + rowt;
+            const int hv = V.hq0 + t;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_ME + b));
+            const bool valid = qv < rv.lq;
+            const bool fin = mbar_wait(bar(BAR_OF + t), kq & 1, abort_flag, a.status, a.wait_ns);
+            if (!__all_sync(0xffffffffu, fin)) break;
+            tc_fence_after();
+            // O = (sum of weights * v codes) * v_scale / (sum of weights); for e4m3
+            // both sums carry the factor 256, which cancels
+            const float inv = l > 0.f ? (kFp8 ? __ldg(a.v_scale + V.h) : 1.f) / l : 0.f;
+            __nv_bfloat16 *dst = a.out + ((long long)(rv.q_off + qv) * bd.h_q + hv) * kHeadDim;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c * 32, o);
-                    tmem_ld_wait();
-                    reg_fence(o);
-                    if (valid) {
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + c * 32, o);
+                tmem_ld_wait();
+                reg_fence(o);
+                if (valid) {
 #pragma unroll
-                        for (int e = 0; e < 32; e += 8) {
-                            uint4 w;
-                            w.x = pack_bf16(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
-                            w.y = pack_bf16(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                            w.z = pack_bf16(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-                            w.w = pack_bf16(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-                            *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
-                        }
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 w;
+                        w.x = pack_bf16(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
+                        w.y = pack_bf16(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                        w.z = pack_bf16(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                        w.w = pack_bf16(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
                     }
                 }
-                if (valid && a.lse)
-                    a.lse[(long long)head * bd.total_q + rq.q_off + qi] =
-                        l > 0.f ? (m + __log2f(l) - (kFp8 ? 8.f : 0.f)) * 0.6931471805599453f : -INFINITY;
             }
-        } else {
-        // a row with no term at all: O = 0, LSE = -inf
-        const int t = (warp - 4) / 4;
-        const int rowt = (warp % 4) * 32 + lane;
-        const int qi = il * kBlock + rowt;
-        if (qi < rq.lq) {
-            const int head = hq0 + t;
-            __nv_bfloat16 *dst = a.out + ((long long)(rq.q_off + qi) * bd.h_q + head) * kHeadDim;
-            for (int c = 0; c < kHeadDim; c += 8) *reinterpret_cast<uint4 *>(dst + c) = make_uint4(0, 0, 0, 0);
-            if (a.lse) a.lse[(long long)head * bd.total_q + rq.q_off + qi] = -INFINITY;
-        }
+            // the next unit's first PV MMA overwrites O only after this warp
+            // group's next P handshake, which follows these reads
+            tc_fence_before();
+            if (valid && a.lse)
+                a.lse[(long long)hv * bd.total_q + rv.q_off + qv] =
+                    l > 0.f ? (m + __log2f(l) - (kFp8 ? 8.f : 0.f)) * 0.6931471805599453f : -INFINITY;
+            ++kq;
         }
     }
 
@@ -512,7 +639,6 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
         tmem_dealloc(tmem, 512);
     }
 }
-
 // ---------------------------------------------------------------------------
 // schedule: units sorted by decreasing work (kept blocks + mean tiles), so the
 // longest rows start first and the tail of the grid is short rows (the
@@ -522,8 +648,9 @@ constexpr int kSchedBins = 4096;
 
 __global__ void __launch_bounds__(1024)
 sched_kernel(const __grid_constant__ BatchDesc bd, const int *__restrict__ row_ptr, int n_pairs,
-             int mean_corr, int *__restrict__ work) {
+             int mean_corr, int *__restrict__ work, int *__restrict__ next_unit) {
     __shared__ int hist[kSchedBins];
+    if (threadIdx.x == 0) *next_unit = 0;
     for (int k = threadIdx.x; k < kSchedBins; k += 1024) hist[k] = 0;
     __syncthreads();
     auto cost = [&](int row) {
@@ -672,12 +799,15 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
         tmKm = tmK;     // never read
         tmVm = tmV;
     }
-    sched_kernel<<<1, 1024, 0, st>>>(bd, L.row_ptr, n_pairs, use_means ? 1 : 0, L.work);
+    int *next_unit = L.work + units;
+    sched_kernel<<<1, 1024, 0, st>>>(bd, L.row_ptr, n_pairs, use_means ? 1 : 0, L.work, next_unit);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail("schedule launch", (int)e);
     AttnArgs a;
     a.row_ptr = L.row_ptr;
     a.col_idx = L.col_idx;
     a.work = L.work;
+    a.next_unit = next_unit;
+    a.n_units = units;
     a.block_table = L.block_table;
     a.max_pages = L.max_pages;
     a.page_size = L.page_size;
@@ -695,7 +825,13 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     auto kern = f8 ? attn_kernel<true> : attn_kernel<false>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttn)) != cudaSuccess)
         return fail("attention smem attribute", (int)e);
-    kern<<<units, kAttnThreads, kSmemAttn, st>>>(bd, tmQ, tmK, tmV, tmKm, tmVm, a);
+    // persistent: one CTA per SM (the shared memory admits one), never more than units
+    int dev = 0, n_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return fail("SM count", (int)e);
+    const int grid = units < n_sm ? units : n_sm;
+    kern<<<grid, kAttnThreads, kSmemAttn, st>>>(bd, tmQ, tmK, tmV, tmKm, tmVm, a);
     if ((e = cudaGetLastError()) != cudaSuccess) {
         if (debug_on()) fprintf(stderr, "[fprefill] attention launch: %s\n", cudaGetErrorString(e));
         return fail("attention launch", (int)e);

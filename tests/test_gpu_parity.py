@@ -104,6 +104,61 @@ def test_random_index_attention_only():
     check_outputs(case, g, oref)
 
 
+@pytest.mark.parametrize("mean_corr", [True, False])
+def test_empty_rows_and_rows_without_their_diagonal_block(mean_corr):
+    """A CSR where every third row is empty and every fifth drops its own
+    (diagonal) block.  With the correction an empty row past block 0 is made
+    of mean tokens only; a row with no term at all gives O = 0, LSE = -inf."""
+    import math
+    import torch
+    import oracle
+    from block_sparse_long_fp_gb300 import fprefill
+    spec = synth.Spec("empty-rows", [(1536, 0), (700, 256), (128, 0)], 8, 2, page_size=32, layout="shuffled",
+                      n_needles=1, config_id=74)
+    case = synth.make_case(spec)
+    rows = synth.random_keep_lists(case, 0.3, seed=7)
+    for k in range(len(rows)):
+        if k % 3 == 0:
+            rows[k] = rows[k][:0]
+        elif k % 5 == 0:
+            rows[k] = rows[k][:-1]
+    row_ptr = np.zeros(len(rows) + 1, np.int32)
+    row_ptr[1:] = np.cumsum([len(x) for x in rows])
+    col_idx = np.concatenate(rows).astype(np.int32)
+    layer = fprefill.layer_from_case(case, params=fprefill.default_params(mean_correction=int(mean_corr)))
+    k_mean, v_mean, _ = layer.discover()
+    out, lse = layer.sparse_attn(torch.from_numpy(row_ptr).cuda(), torch.from_numpy(col_idx).cuda(), k_mean,
+                                 v_mean)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    got_o, got_l = out.float().cpu().numpy(), lse.cpu().numpy()
+    k = 0
+    n_void = 0
+    for r, (lq, start) in enumerate(spec.requests):
+        q = oracle.request_q(case, r)
+        kk, vv = oracle.request_kv(case, r)
+        kbar, vbar = oracle.pool(kk, 128), oracle.pool(vv, 128)
+        nqb = -(-lq // 128)
+        keep = np.zeros((nqb, spec.h_kv, kbar.shape[0]), np.uint8)
+        for i in range(nqb):
+            for h in range(spec.h_kv):
+                keep[i, h, rows[k]] = 1
+                k += 1
+        qi = np.repeat(np.arange(lq), spec.h_q)
+        qh = np.tile(np.arange(spec.h_q), lq)
+        o, l = oracle.attn_rows(q, start, kk, vv, kbar, vbar, 128, 1 / math.sqrt(128), keep, mean_corr, qi, qh)
+        q0 = int(case.cu_seqlens_q[r])
+        go, gl = got_o[q0 + qi, qh], got_l[qh, q0 + qi]
+        void = np.isneginf(l)
+        n_void += int(void.sum())
+        assert np.array_equal(np.isneginf(gl), void), r
+        assert np.all(go[void] == 0.0), r
+        err = np.abs(go[~void] - o[~void])
+        assert err.max() <= 2e-2 and err.mean() <= 2e-3, (r, err.max(), err.mean())
+        assert np.abs(gl[~void] - l[~void]).max() <= 2e-2, r
+    assert n_void > 0
+
+
 def test_dense_path_equals_causal_softmax():
     import oracle
     spec = synth.Spec("dense", [(1000, 0), (384, 256)], 4, 2, page_size=64, layout="shuffled",
