@@ -12,9 +12,10 @@
 // How (sm_103a design, not the Hopper one of the pages):
 //  * a work unit = (index row (request, query block I, kv head h), a pair of
 //    query heads of the group): two 128-query tiles Q0, Q1;
-//  * persistent CTAs, one per SM, take units off a list sorted by decreasing
-//    work; warp 2 prepares the next unit's metadata (kept-block bitmap, mean
-//    tiles) while the current one runs;
+//  * persistent CTAs, one per SM, take units off a list grouped by (request,
+//    kv head) for L2 reuse, longest rows first; warp 2 prepares the next
+//    unit's metadata (kept-block bitmap, mean tiles) while the current one
+//    runs;
 //  * warp 0 issues TMA loads (Q once; K and V tiles through the page table
 //    into a two-stage ring each; mean tiles from the bf16 copies of the block
 //    means);
@@ -83,7 +84,7 @@ static_assert(sizeof(UnitMeta) % 16 == 0, "metadata buffers");
 struct AttnArgs {
     const int *row_ptr;       // null in dense mode
     const int *col_idx;
-    const int *work;          // unit ids sorted by decreasing work
+    const int *work;          // unit ids in schedule order
     int *next_unit;           // work-list cursor (zeroed by the schedule kernel)
     int n_units;
     const int *block_table;
@@ -135,8 +136,8 @@ __device__ __forceinline__ Unit decode_unit(const BatchDesc &bd, const AttnArgs 
 // 256 * p (the scaling of the V2 paper reading, section 4.2 (4), which keeps
 // the weights in e4m3's normal range; it cancels in the ratio).
 //
-// Persistent: one CTA per SM walks the work list (a shared cursor, so the
-// longest units go first and each SM takes the next unit when it is ready).
+// Persistent: one CTA per SM walks the work list (a shared cursor: each SM
+// takes the next unit when it is ready).
 // Barrier phases run on counters that span units: `it` counts the CTA's
 // items (K/V ring slots, S and P handshakes), `kq` its non-empty units (Q and
 // O handshakes), `k` all its units (metadata buffers).  The next unit's Q,
@@ -640,40 +641,93 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
     }
 }
 // ---------------------------------------------------------------------------
-// schedule: units sorted by decreasing work (kept blocks + mean tiles), so the
-// longest rows start first and the tail of the grid is short rows (the
-// kept-count load balancing of the V2 popular article, "KV split").
+// schedule: the order in which the persistent CTAs take units.  Units are
+// grouped by (request, kv head), so the units in flight share one head's K and
+// V (64 MB for a 128K request) and hit L2 instead of re-reading DRAM; groups
+// go by decreasing row length (the requests with the longest rows first, kv
+// heads in order), and inside a group rows go by decreasing work (kept blocks
+// plus mean tiles), so the tail of the launch is short rows (the kept-count
+// load balancing of the V2 popular article, "KV split").  One CTA per group:
+// a counting sort of its rows by work.
 // ---------------------------------------------------------------------------
 constexpr int kSchedBins = 4096;
+constexpr int kSchedThreads = 1024;
 
-__global__ void __launch_bounds__(1024)
-sched_kernel(const __grid_constant__ BatchDesc bd, const int *__restrict__ row_ptr, int n_pairs,
-             int mean_corr, int *__restrict__ work, int *__restrict__ next_unit) {
+__global__ void __launch_bounds__(kSchedThreads)
+sched_kernel(const __grid_constant__ BatchDesc bd, const int *__restrict__ row_ptr, int n_pairs, int mean_corr,
+             int *__restrict__ work, int *__restrict__ next_unit) {
     __shared__ int hist[kSchedBins];
-    if (threadIdx.x == 0) *next_unit = 0;
-    for (int k = threadIdx.x; k < kSchedBins; k += 1024) hist[k] = 0;
-    __syncthreads();
-    auto cost = [&](int row) {
-        const int r = req_of_row(bd, row);
-        const ReqDesc &rq = bd.req[r];
-        const int I = rq.start / kBlock + (row - rq.row_base) / bd.h_kv;
-        int c = row_ptr ? row_ptr[row + 1] - row_ptr[row] + (mean_corr ? (I + kBlock - 1) / kBlock : 0) : I + 1;
-        return min(c, kSchedBins - 1);
-    };
-    for (int row = threadIdx.x; row < bd.total_rows; row += 1024) atomicAdd(&hist[cost(row)], 1);
-    __syncthreads();
-    if (threadIdx.x == 0) {        // descending exclusive scan (4096 bins, once)
-        int run = 0;
-        for (int k = kSchedBins - 1; k >= 0; --k) {
-            int v = hist[k];
-            hist[k] = run;
-            run += v;
+    __shared__ int warp_sum[kSchedThreads / 32];
+    __shared__ int grp[3];                          // request, kv head, first position of the group
+    const int tid = threadIdx.x, lane = tid % 32, wid = tid / 32;
+    if (tid == 0) {
+        if (blockIdx.x == 0) *next_unit = 0;
+        int ord[FP_MAX_BATCH];
+        for (int r = 0; r < bd.batch; ++r) {          // insertion sort: nkb descending, index ascending
+            int k = r;
+            while (k > 0 && bd.req[ord[k - 1]].nkb < bd.req[r].nkb) {
+                ord[k] = ord[k - 1];
+                --k;
+            }
+            ord[k] = r;
         }
+        const int rank = blockIdx.x / bd.h_kv, h = blockIdx.x % bd.h_kv;
+        int base = 0;
+        for (int k = 0; k < rank; ++k) base += bd.req[ord[k]].nqb * bd.h_kv * n_pairs;
+        const int r = ord[rank];
+        grp[0] = r;
+        grp[1] = h;
+        grp[2] = base + h * bd.req[r].nqb * n_pairs;
+    }
+    for (int k = tid; k < kSchedBins; k += kSchedThreads) hist[k] = 0;
+    __syncthreads();
+    const ReqDesc &rq = bd.req[grp[0]];
+    const int h = grp[1], base = grp[2];
+    auto cost = [&](int il) {
+        const int row = rq.row_base + il * bd.h_kv + h;
+        const int I = rq.start / kBlock + il;
+        const int c = row_ptr ? row_ptr[row + 1] - row_ptr[row] + (mean_corr ? (I + kBlock - 1) / kBlock : 0) : I + 1;
+        return kSchedBins - 1 - min(c, kSchedBins - 1);     // bin 0 = the most work
+    };
+    for (int il = tid; il < rq.nqb; il += kSchedThreads) atomicAdd(&hist[cost(il)], 1);
+    __syncthreads();
+    // exclusive scan of the bins: four consecutive bins per thread, then the block
+    constexpr int kPer = kSchedBins / kSchedThreads;
+    int v[kPer], run = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        v[k] = hist[tid * kPer + k];
+        run += v[k];
+    }
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sum[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int w = warp_sum[lane], wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        warp_sum[lane] = wi - w;                    // exclusive prefix of the warps
     }
     __syncthreads();
-    for (int row = threadIdx.x; row < bd.total_rows; row += 1024) {
-        int slot = atomicAdd(&hist[cost(row)], 1);
-        for (int p = 0; p < n_pairs; ++p) work[slot * n_pairs + p] = row * n_pairs + p;
+    int pre = warp_sum[wid] + incl - run;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        hist[tid * kPer + k] = pre;
+        pre += v[k];
+    }
+    __syncthreads();
+    for (int il = tid; il < rq.nqb; il += kSchedThreads) {
+        const int slot = atomicAdd(&hist[cost(il)], 1);
+        const int row = rq.row_base + il * bd.h_kv + h;
+        for (int p = 0; p < n_pairs; ++p) work[base + slot * n_pairs + p] = row * n_pairs + p;
     }
 }
 
@@ -800,7 +854,8 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
         tmVm = tmV;
     }
     int *next_unit = L.work + units;
-    sched_kernel<<<1, 1024, 0, st>>>(bd, L.row_ptr, n_pairs, use_means ? 1 : 0, L.work, next_unit);
+    sched_kernel<<<bd.batch * bd.h_kv, kSchedThreads, 0, st>>>(bd, L.row_ptr, n_pairs, use_means ? 1 : 0, L.work,
+                                                              next_unit);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail("schedule launch", (int)e);
     AttnArgs a;
     a.row_ptr = L.row_ptr;
