@@ -20,9 +20,13 @@
 // chunk of key blocks, shared by both heads, in a ring of stages), warp 1
 // issues the MMAs, warpgroup A (warps 4-7) and warpgroup B (warps 8-11) each
 // own one head of the pair and its TMEM S buffers, one query row per thread,
-// so the two heads' row work overlaps.  Each warpgroup also writes its head's
-// query tile into TMEM, where the MMA takes it as the A operand: the MMAs read
-// only the mean terms from shared memory.
+// so the two heads' row work overlaps.  A row warp pulls a whole chunk of S
+// into registers before it works on it, so the buffer is free for the next
+// MMA at once.  Each warpgroup also writes its head's query tile into TMEM,
+// where the MMA takes it as the A operand (the MMAs read only the mean terms
+// from shared memory); there are two query buffers, and the next pair's
+// queries (prefetched into L2 when the pair starts) go in at the start of
+// this pair's second pass, so the tensor cores never wait for them.
 #include "common.cuh"
 #include "launch.cuh"
 #include "sm100.cuh"
@@ -34,7 +38,6 @@ using namespace sm100;
 namespace {
 
 constexpr int kScThreads = 384;
-constexpr int kQBytes = kBlock * kHeadDim * 2;             // 32 KB
 
 // Layout of one build of the kernel for a chunk of kChunk key blocks (MMA N):
 // 128-block chunks halve the MMA instructions per FLOP (measured 2.9 vs 4.0
@@ -51,13 +54,16 @@ struct ScoreCfg {
     static constexpr int kSmStage = 0;
     static constexpr int kSmCtl = kSmStage + kStages * kStageBytes;
     static constexpr int kSmAcc = kSmCtl + 256;                // per-warp column sums [8][max_nkb]
-    // TMEM: the S buffers (kBufs per head slot), then the two query tiles as
-    // MMA A operands (128 rows x 128 bf16 = 64 columns each)
+    // TMEM: the S buffers (kBufs per head slot), then the query tiles as MMA
+    // A operands (128 rows x 128 bf16 = 64 columns each), two buffers of two
+    // head slots, so the next pair's queries go in while this pair runs
     static constexpr int kTmemQ = kTmemBufs * C;
-    // barriers: Q full/empty per head slot, stage full/empty, TMEM full/empty per (slot, buffer)
-    static constexpr int B_QF = 0, B_QE = 2, B_SF = 4, B_SE = 4 + kStages, B_TF = 4 + 2 * kStages;
+    // barriers: Q full/empty per (buffer, head slot), stage full/empty, TMEM
+    // full/empty per (head slot, S buffer)
+    static constexpr int B_QF = 0, B_QE = 4, B_SF = 8, B_SE = 8 + kStages, B_TF = 8 + 2 * kStages;
     static constexpr int B_TE = B_TF + 4, B_N = B_TE + 4;
-    static_assert(kTmemQ + 128 <= 512, "TMEM budget");
+    static_assert(kTmemQ + 256 <= 512, "TMEM budget");
+    static_assert(B_N * 8 + 64 <= 256, "control block");
     static size_t smem_bytes(int max_nkb) { return (size_t)kSmAcc + 8 * sizeof(float) * max_nkb + 1024; }
 };
 
@@ -191,7 +197,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < B_N; ++k)
-            mbar_init(bar(k), ((k >= B_TE && k < B_TE + 4) || (k >= B_QF && k < B_QF + 2)) ? 128u : 1u);
+            mbar_init(bar(k), ((k >= B_TE && k < B_TE + 4) || (k >= B_QF && k < B_QF + 4)) ? 128u : 1u);
         *abort_flag = 0;
         *sync_ctr = 0u;
         fence_barrier_init();
@@ -206,9 +212,9 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ================= TMA producer =================
-        if (lane == 0) {
+    if (warp < 4) {
+        if (warp == 0 && lane == 0) {
+            // ================= TMA producer =================
             tma_prefetch_desc(&tmM);
             int step = 0;
             for (int pr = 0; pr < npairs && !*abort_flag; ++pr) {
@@ -226,17 +232,17 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                 }
             }
         producer_done:;
-        }
-    } else if (warp == 1) {
-        // ================= MMA issuer =================
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
+            // ================= MMA issuer =================
             constexpr uint32_t idS = idesc_bf16(128, kChunk, false);
             int step = 0;
             int uses[2] = {0, 0};                  // TMEM-buffer uses per head slot
             for (int pr = 0; pr < npairs; ++pr) {
                 const int nw = (2 * pr + 1 < g) ? 2 : 1;
+                const int qb = pr & 1;             // query buffer of this pair
                 for (int w = 0; w < nw; ++w)
-                    if (!mbar_wait(bar(B_QF + w), pr & 1, abort_flag, a.status, a.wait_ns)) goto mma_done;
+                    if (!mbar_wait(bar(B_QF + 2 * qb + w), (pr >> 1) & 1, abort_flag, a.status, a.wait_ns))
+                        goto mma_done;
                 for (int k = 0; k < steps_per_pair; ++k, ++step) {
                     const int s = step % kStages;
                     if (!mbar_wait(bar(B_SF + s), (step / kStages) & 1, abort_flag, a.status, a.wait_ns)) goto mma_done;
@@ -251,7 +257,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                         // descriptors differ only in the start address: add offsets (in 16-byte units)
                         const uint64_t kd = smem_desc_sw128(kb, 16, 1024);
                         const uint32_t dt = tmem + (kBufs * w + b) * kChunk;
-                        const uint32_t qt = tmem + kTmemQ + w * 64;          // A: 16 d-values per 8 columns
+                        const uint32_t qt = tmem + kTmemQ + (2 * qb + w) * 64;   // A: 16 d-values per 8 columns
 #pragma unroll
                         for (int t = 0; t < 3; ++t)
 #pragma unroll
@@ -263,11 +269,11 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                     }
                     tc_commit(bar(B_SE + s));
                 }
-                for (int w = 0; w < nw; ++w) tc_commit(bar(B_QE + w));
+                for (int w = 0; w < nw; ++w) tc_commit(bar(B_QE + 2 * qb + w));
             }
         mma_done:;
         }
-    } else if (warp >= 4) {
+    } else {
         // ================= row warpgroups: one head each, one query row per thread =================
         const int w = (warp - 4) / 4;                     // head slot of the pair
         const int quarter = warp % 4;
@@ -280,88 +286,116 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
         int u = 0;
         bool ok = true;
         unsigned gen = 0;
+        // head hq's query rows -> query buffer qb in TMEM as the MMA's A operand
+        // (e4m3 codes are converted exactly to bf16); 32 columns = 64 values at
+        // a time.  Returns false if the CTA is aborting.
+        auto put_queries = [&](int pr_q) -> bool {
+            const int qb = pr_q & 1;
+            if (pr_q >= 2) {                       // the buffer's previous pair is done with it
+                const bool got = mbar_wait(bar(B_QE + 2 * qb + w), ((pr_q >> 1) & 1) ^ 1, abort_flag, a.status,
+                                           a.wait_ns);
+                if (!__all_sync(0xffffffffu, got)) return false;
+            }
+            const int hq = h * g + 2 * pr_q + w;
+            const long long el = (long long)(rq.q_off + il * kBlock + rowt) * a.q_stride_tok + (long long)hq * a.q_stride_head;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t qw[32];
+                if constexpr (!kFp8) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(a.q16 + el) + half * 8;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const uint4 c = row_valid ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                        qw[4 * v] = c.x; qw[4 * v + 1] = c.y; qw[4 * v + 2] = c.z; qw[4 * v + 3] = c.w;
+                    }
+                } else {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(a.q8 + el) + half * 4;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const uint4 c = row_valid ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const __nv_fp8x2_storage_t c2v = (__nv_fp8x2_storage_t)(cw[k / 2] >> (16 * (k & 1)));
+                            const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(c2v, __NV_E4M3)));
+                            qw[8 * v + k] = pack_bf16x2(f.x, f.y);
+                        }
+                    }
+                }
+                tmem_st32(lane_base + kTmemQ + (2 * qb + w) * 64 + half * 32, qw);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(B_QF + 2 * qb + w));
+            return true;
+        };
+        // the next pair's query row into L2 ahead of its load (bf16: two 128-byte lines)
+        auto prefetch_queries = [&](int pr_q) {
+            if (!row_valid) return;
+            const int hq = h * g + 2 * pr_q + w;
+            const long long el = (long long)(rq.q_off + il * kBlock + rowt) * a.q_stride_tok + (long long)hq * a.q_stride_head;
+            const size_t p = __cvta_generic_to_global(kFp8 ? static_cast<const void *>(a.q8 + el)
+                                                           : static_cast<const void *>(a.q16 + el));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+            if constexpr (!kFp8) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + 128));
+        };
+        if (w < g) ok = put_queries(0);
         for (int pr = 0; pr < npairs && ok; ++pr) {
             if (2 * pr + w >= g) break;
             const int hq = h * g + 2 * pr + w;
+            const bool next = 2 * (pr + 1) + w < g;       // this slot has a head in the next pair
+            if (next) prefetch_queries(pr + 1);
             const float c2 = kFp8 ? a.scale_log2 * __ldg(a.q_scale + hq) : a.scale_log2;
-            {
-                // this head's query rows -> TMEM as the MMA's A operand (e4m3 codes
-                // are converted exactly to bf16); 32 columns = 64 values at a time
-                if (pr >= 1) {
-                    const bool got = mbar_wait(bar(B_QE + w), (pr - 1) & 1, abort_flag, a.status, a.wait_ns);
-                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-                }
-                const int qi = il * kBlock + rowt;
-                const long long el = (long long)(rq.q_off + qi) * a.q_stride_tok + (long long)hq * a.q_stride_head;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t qw[32];
-                    if constexpr (!kFp8) {
-                        const uint4 *src = reinterpret_cast<const uint4 *>(a.q16 + el) + half * 8;
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            const uint4 c = row_valid ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-                            qw[4 * v] = c.x; qw[4 * v + 1] = c.y; qw[4 * v + 2] = c.z; qw[4 * v + 3] = c.w;
-                        }
-                    } else {
-                        const uint4 *src = reinterpret_cast<const uint4 *>(a.q8 + el) + half * 4;
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const uint4 c = row_valid ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-                            const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                const __nv_fp8x2_storage_t c2v = (__nv_fp8x2_storage_t)(cw[k / 2] >> (16 * (k & 1)));
-                                const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(c2v, __NV_E4M3)));
-                                qw[8 * v + k] = pack_bf16x2(f.x, f.y);
-                            }
-                        }
-                    }
-                    tmem_st32(lane_base + kTmemQ + w * 64 + half * 32, qw);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(bar(B_QF + w));
-            }
             float m = -INFINITY;
             float mc2 = 0.f;
             for (int pass = 0; pass < 2 && ok; ++pass) {
-                if (pass == 1) mc2 = (m == -INFINITY || !row_valid) ? 0.f : m * c2;
+                if (pass == 1) {
+                    mc2 = (m == -INFINITY || !row_valid) ? 0.f : m * c2;
+                    // the next pair's queries go into the other buffer while this
+                    // pair's second pass keeps the tensor cores busy
+                    if (next && !put_queries(pr + 1)) { ok = false; break; }
+                }
                 for (int c = 0; c < nch; ++c, ++u) {
                     const int b = u % kBufs;
                     const bool got = mbar_wait(bar(B_TF + kBufs * w + b), (u / kBufs) & 1, abort_flag, a.status,
                                                a.wait_ns);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     tc_fence_after();
+                    // the whole chunk into registers, then the buffer is free for
+                    // the next MMA while this warp works on the values
                     const uint32_t colb = lane_base + (kBufs * w + b) * kChunk;
-                    float m4[4] = {m, -INFINITY, -INFINITY, -INFINITY};
+                    uint32_t sv[kChunk / 32][32];
 #pragma unroll
-                    for (int sl = 0; sl < kChunk / 32; ++sl) {
-                        uint32_t u0[32];
-                        tmem_ld32(colb + sl * 32, u0);
-                        tmem_ld_wait();
-                        reg_fence(u0);
-                        if (sl == kChunk / 32 - 1) {           // the buffer is free once read
-                            tc_fence_before();
-                            mbar_arrive(bar(B_TE + kBufs * w + b));
-                        }
-                        const int J0 = c * kChunk + sl * 32;
-                        if (pass == 0) {
+                    for (int sl = 0; sl < kChunk / 32; ++sl) tmem_ld32(colb + sl * 32, sv[sl]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int sl = 0; sl < kChunk / 32; ++sl) reg_fence(sv[sl]);
+                    tc_fence_before();
+                    mbar_arrive(bar(B_TE + kBufs * w + b));
+                    if (pass == 0) {
+                        float m4[4] = {m, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                        for (int sl = 0; sl < kChunk / 32; ++sl) {
+                            const int J0 = c * kChunk + sl * 32;
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
-                                if (J0 + e < ncol) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(u0[e]));
-                        } else {
+                                if (J0 + e < ncol) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sv[sl][e]));
+                        }
+                        m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    } else {
+#pragma unroll
+                        for (int sl = 0; sl < kChunk / 32; ++sl) {
+                            const int J0 = c * kChunk + sl * 32;
                             float v0[32];
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
-                                v0[e] = (row_valid && J0 + e < ncol) ? fast_exp2(fmaf(__uint_as_float(u0[e]), c2, -mc2))
+                                v0[e] = (row_valid && J0 + e < ncol) ? fast_exp2(fmaf(__uint_as_float(sv[sl][e]), c2, -mc2))
                                                                       : 0.f;
                             // lane L now gets the sum of column J0 + L over this warp's 32 rows
                             const float s0 = transpose_reduce32(v0, lane);
                             if (J0 + lane < ncol) my_acc[J0 + lane] += s0;
                         }
                     }
-                    if (pass == 0) m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 }
             }
         }
