@@ -519,39 +519,27 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     m = mx;
                 }
                 const float off = bias - (m == -INFINITY ? 0.f : m);
-                float rs;
-                // exponents as paired FMAs: (s0, s1) * c + off
+                // exponents as paired FMAs: (s0, s1) * c + off.  P goes to TMEM
+                // first; the denominator is summed from the packed registers after
+                // the MMA has been told P is ready, off the critical path.
                 const uint64_t cc = f2_pack(csc, csc);
+                constexpr int kPk = kFp8 ? 32 : 64;   // packed words of P per row
+                uint32_t pk[kPk];
                 if constexpr (!kFp8) {
                     const uint64_t oo = f2_pack(off, off);
-                    uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
-                        uint32_t pk[32];
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
                             float z0, z1;
                             f2_unpack(f2_fma(f2_pack(x[64 * half + 2 * e], x[64 * half + 2 * e + 1]), cc, oo), z0, z1);
-                            pk[e] = pack_bf16(fast_exp2(z0), fast_exp2(z1));
-                            // the denominator sums the same bf16-rounded weights the MMA
-                            // multiplies, so the weights of a row sum to exactly one
-                            acc2[e & 1] = f2_add(acc2[e & 1], f2_pack(__uint_as_float(pk[e] << 16),
-                                                                      __uint_as_float(pk[e] & 0xffff0000u)));
+                            pk[32 * half + e] = pack_bf16(fast_exp2(z0), fast_exp2(z1));
                         }
-                        tmem_st32(tS + 32 * half, pk);
+                        tmem_st32(tS + 32 * half, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * half));
                     }
-                    float r0, r1, r2, r3;
-                    f2_unpack(acc2[0], r0, r1);
-                    f2_unpack(acc2[1], r2, r3);
-                    rs = (r0 + r1) + (r2 + r3);
                 } else {
-                    // e4m3 of 256 * p: four weights per TMEM column; the denominator
-                    // sums the decoded weights (in half2, <= 128 * 256 < 65504)
+                    // e4m3 of 256 * p: four weights per TMEM column
                     const uint64_t oo = f2_pack(off + 8.f, off + 8.f);
-                    uint32_t pk[32];
-                    __half2 hs[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) hs[q] = __float2half2_rn(0.f);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         float z0, z1, z2, z3;
@@ -562,15 +550,9 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
                             make_float2(fast_exp2(z2), fast_exp2(z3)), __NV_SATFINITE, __NV_E4M3);
                         pk[e] = (uint32_t)lo | ((uint32_t)hi << 16);
-                        hs[e & 3] = __hadd2(hs[e & 3], __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3)),
-                                                               __half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3))));
                     }
-                    tmem_st32(tS, pk);
-                    const float2 f0 = __half22float2(hs[0]), f1 = __half22float2(hs[1]);
-                    const float2 f2 = __half22float2(hs[2]), f3 = __half22float2(hs[3]);
-                    rs = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
+                    tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(pk));
                 }
-                l += rs;
                 if (any_grow && j > 0) {
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
@@ -586,6 +568,36 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar(BAR_PF + t));
+                // the denominator sums the same rounded weights the MMA multiplies,
+                // so the weights of a row sum to exactly one
+                float rs;
+                if constexpr (!kFp8) {
+                    uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+                    for (int e = 0; e < 64; ++e)
+                        acc2[e & 1] = f2_add(acc2[e & 1], f2_pack(__uint_as_float(pk[e] << 16),
+                                                                  __uint_as_float(pk[e] & 0xffff0000u)));
+                    float r0, r1, r2, r3;
+                    f2_unpack(acc2[0], r0, r1);
+                    f2_unpack(acc2[1], r2, r3);
+                    rs = (r0 + r1) + (r2 + r3);
+                } else {
+                    // decoded e4m3 weights summed in half2 (<= 128 * 256 < 65504)
+                    __half2 hs[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) hs[q] = __float2half2_rn(0.f);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const __nv_fp8x2_storage_t lo = (__nv_fp8x2_storage_t)(pk[e] & 0xffffu);
+                        const __nv_fp8x2_storage_t hi = (__nv_fp8x2_storage_t)(pk[e] >> 16);
+                        hs[e & 3] = __hadd2(hs[e & 3], __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3)),
+                                                               __half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3))));
+                    }
+                    const float2 f0 = __half22float2(hs[0]), f1 = __half22float2(hs[1]);
+                    const float2 f2 = __half22float2(hs[2]), f3 = __half22float2(hs[3]);
+                    rs = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
+                }
+                l += rs;
             }
             if (!ok) break;
             // epilogue: O / l -> bf16, LSE.  The unit's fields are decoded again
