@@ -251,75 +251,124 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 mbar_arrive(bar(BAR_MF + b));
                 if (end) break;
             }
-        } else if (warp == 0 && lane == 0) {
+        } else if (warp == 0) {
             // ================= TMA producer =================
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
+            // Lane 0 waits on the rings and issues the copies.  The page-table
+            // lookups (the index entry, then the page of each sub-box) are done
+            // by the whole warp, one round of 32 / nsub items at a time, a round
+            // ahead, so their latency hides behind the copies of the round
+            // before; K and V of an item share them.
+            if (lane == 0) {
+                tma_prefetch_desc(&tmQ);
+                tma_prefetch_desc(&tmK);
+                tma_prefetch_desc(&tmV);
+            }
             const int rpb = a.page_size < kBlock ? a.page_size : kBlock;   // rows per box
+            const int nsub = kBlock / rpb;                                 // boxes per tile: 1, 2, 4 or 8
+            const int per = 32 / nsub;                                     // items per lookup round
             const int oob = a.num_pages * a.page_size;                     // zero-filled rows
             uint32_t it = 0;
             int kq = 0;
             for (int k = 0;; ++k) {
                 const int b = k & 1;
                 const UnitMeta &M = meta[b];
-                if (!mbar_wait(bar(BAR_MF + b), (k >> 1) & 1, abort_flag, a.status, a.wait_ns)) break;
+                bool got = true;
+                if (lane == 0) got = mbar_wait(bar(BAR_MF + b), (k >> 1) & 1, abort_flag, a.status, a.wait_ns);
+                if (!__shfl_sync(0xffffffffu, got, 0)) break;
+                __syncwarp();                               // lane 0's acquire covers the warp's reads
                 if (M.pos < 0) break;
                 const int n_items = M.n_items;
                 if (n_items > 0) {
                     const Unit U = decode_unit(bd, a, M.unit);
                     const ReqDesc &rq = bd.req[U.r];
-                    // Q of the previous unit is free once its last S MMAs are done
-                    if (kq > 0 && !mbar_wait(bar(BAR_QE), (kq - 1) & 1, abort_flag, a.status, a.wait_ns)) break;
-                    const int q_row0 = rq.q_off + U.il * kBlock;
-                    mbar_expect_tx(bar(BAR_Q), 2 * kT);
-                    for (int t = 0; t < 2; ++t)
-                        for (int hf = 0; hf < kNH; ++hf)
-                            tma_load_3d(sbase + kSmemQ + t * kTileBytes + hf * kHalfBytes, &tmQ, bar(BAR_Q),
-                                        hf * 64, U.hq0 + t, q_row0);
                     const int *bt = a.block_table + (long long)U.r * a.max_pages;
                     const int npages_req = (rq.lk + a.page_size - 1) / a.page_size;
+                    // this lane's lookup for item j0 + lane / nsub, box lane % nsub:
+                    // the page id (in flight until used) and the row inside the page;
+                    // page -1: past the request (zero fill), -2: not a kept item
+                    auto look = [&](int j0, int &pg, int &off) {
+                        const int jj = j0 + lane / nsub;
+                        pg = -2;
+                        off = 0;
+                        if (jj < U.n_kept) {
+                            const int J = sparse ? __ldg(a.col_idx + U.rp0 + jj) : jj;
+                            const int tok = J * kBlock + (lane % nsub) * rpb;
+                            const int lp = tok / a.page_size;
+                            off = tok % a.page_size;
+                            pg = (tok < rq.lk && lp < npages_req) ? __ldg(bt + lp) : -1;
+                        }
+                    };
+                    // row of the paged pool a looked-up box starts at
+                    auto row_of = [&](int pg, int off) {
+                        if (pg == -1 || pg == -2) return oob;
+                        if (pg < 0 || pg >= a.num_pages) {
+                            set_status(a.status, FP_ERR_DEVICE_BOUNDS);
+                            return oob;
+                        }
+                        return pg * a.page_size + off;
+                    };
                     bool good = true;
-                    for (int j = 0; j < n_items && good; ++j, ++it) {
-                        const int s = it & 1, ph = (it >> 1) & 1;
-                        const bool kept = j < U.n_kept;
-                        int J = 0, c = 0;
-                        if (kept) J = sparse ? __ldg(a.col_idx + U.rp0 + j) : j;
-                        else c = M.corr[j - U.n_kept];
-                        for (int op = 0; op < 2; ++op) {       // 0: K tile, 1: V tile
-                            const uint32_t full = bar(op == 0 ? BAR_KF + s : BAR_VF + s);
-                            if (it >= 2 && !mbar_wait(bar(op == 0 ? BAR_KE + s : BAR_VE + s), ph ^ 1, abort_flag,
-                                                      a.status, a.wait_ns)) {
-                                good = false;
-                                break;
-                            }
-                            const uint32_t dst = sbase + (op == 0 ? kSmemK : kSmemV) + s * kTileBytes;
-                            mbar_expect_tx(full, kT);
-                            if (kept) {
-                                const CUtensorMap *tm = op == 0 ? &tmK : &tmV;
-                                for (int sub = 0; sub < kBlock / rpb; ++sub) {
-                                    const int tok = J * kBlock + sub * rpb;
-                                    int z = oob;
-                                    const int lp = tok / a.page_size;
-                                    if (tok < rq.lk && lp < npages_req) {
-                                        const int pg = __ldg(bt + lp);
-                                        if (pg >= 0 && pg < a.num_pages) z = pg * a.page_size + tok % a.page_size;
-                                        else set_status(a.status, FP_ERR_DEVICE_BOUNDS);
-                                    }
-                                    for (int hf = 0; hf < kNH; ++hf)
-                                        tma_load_3d(dst + hf * kHalfBytes + sub * rpb * 128, tm, full, hf * 64, U.h, z);
-                                }
-                            } else {
-                                const CUtensorMap *tm = op == 0 ? &tmKm : &tmVm;
+                    if (lane == 0) {
+                        // Q of the previous unit is free once its last S MMAs are done
+                        if (kq > 0 && !mbar_wait(bar(BAR_QE), (kq - 1) & 1, abort_flag, a.status, a.wait_ns)) good = false;
+                        if (good) {
+                            const int q_row0 = rq.q_off + U.il * kBlock;
+                            mbar_expect_tx(bar(BAR_Q), 2 * kT);
+                            for (int t = 0; t < 2; ++t)
                                 for (int hf = 0; hf < kNH; ++hf)
-                                    tma_load_3d(dst + hf * kHalfBytes, tm, full, hf * 64, U.h, rq.kb_base + c * kBlock);
+                                    tma_load_3d(sbase + kSmemQ + t * kTileBytes + hf * kHalfBytes, &tmQ, bar(BAR_Q),
+                                                hf * 64, U.hq0 + t, q_row0);
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, good, 0)) break;
+                    int pg_n, off_n;
+                    look(0, pg_n, off_n);
+                    int z_cur = oob;
+                    for (int j = 0; j < n_items && good; ++j, ++it) {
+                        const int lj = j % per;
+                        if (lj == 0) {                      // next round: take it, look up the one after
+                            z_cur = row_of(pg_n, off_n);
+                            look(j + per, pg_n, off_n);
+                        }
+                        const bool kept = j < U.n_kept;
+                        int zs[8];
+#pragma unroll
+                        for (int sub = 0; sub < 8; ++sub)
+                            zs[sub] = __shfl_sync(0xffffffffu, z_cur, (lj * nsub + sub) & 31);
+                        if (lane == 0) {
+                            const int s = it & 1, ph = (it >> 1) & 1;
+                            const int c = kept ? 0 : M.corr[j - U.n_kept];
+                            for (int op = 0; op < 2 && good; ++op) {       // 0: K tile, 1: V tile
+                                const uint32_t full = bar(op == 0 ? BAR_KF + s : BAR_VF + s);
+                                if (it >= 2 && !mbar_wait(bar(op == 0 ? BAR_KE + s : BAR_VE + s), ph ^ 1, abort_flag,
+                                                          a.status, a.wait_ns)) {
+                                    good = false;
+                                    break;
+                                }
+                                const uint32_t dst = sbase + (op == 0 ? kSmemK : kSmemV) + s * kTileBytes;
+                                mbar_expect_tx(full, kT);
+                                if (kept) {
+                                    const CUtensorMap *tm = op == 0 ? &tmK : &tmV;
+#pragma unroll
+                                    for (int sub = 0; sub < 8; ++sub)
+                                        if (sub < nsub)
+                                            for (int hf = 0; hf < kNH; ++hf)
+                                                tma_load_3d(dst + hf * kHalfBytes + sub * rpb * 128, tm, full, hf * 64,
+                                                            U.h, zs[sub]);
+                                } else {
+                                    const CUtensorMap *tm = op == 0 ? &tmKm : &tmVm;
+                                    for (int hf = 0; hf < kNH; ++hf)
+                                        tma_load_3d(dst + hf * kHalfBytes, tm, full, hf * 64, U.h, rq.kb_base + c * kBlock);
+                                }
                             }
                         }
+                        good = __shfl_sync(0xffffffffu, good, 0);
                     }
                     if (!good) break;
                     ++kq;
                 }
-                mbar_arrive(bar(BAR_ME + b));
+                __syncwarp();                               // the warp's reads of the metadata are done
+                if (lane == 0) mbar_arrive(bar(BAR_ME + b));
             }
         } else if (warp == 1 && lane == 0) {
             // ================= MMA issuer =================
