@@ -241,6 +241,27 @@ def summary(m, spec, logit_scale, dtype):
     }
 
 
+def chunk_variant(dev, stream, steps, dense_steps):
+    """A chunked-prefill step at long context: 512 queries at position 130560
+    (32/4 heads, the 128K layer's shape).  It has 64 work units for 152 SMs, so
+    the attention splits each row's key list (split-KV) and merges the parts by
+    LSE; timed with the automatic split and with splitting off."""
+    from block_sparse_long_fp_gb300 import fprefill, synth
+    spec = synth.Spec("chunk-512-at-128k", [(512, 130560)], 32, 4, page_size=64, layout="shuffled", n_needles=4,
+                      config_id=6)
+    case = synth.make_case(spec)
+    out = {"workload": spec.name}
+    for name, ks in (("auto_split", 0), ("no_split", 1)):
+        layer = fprefill.layer_from_case(case, device=dev, params=fprefill.default_params(kv_splits=ks))
+        res = summary(measure_layer(layer, spec, steps, 2, dense_steps, stream), spec, 1.0, "bf16")
+        res["kv_splits"] = layer.kv_splits
+        out[name] = res
+        del layer
+    a, n = out["auto_split"]["stages_ms"]["sparse_attn"], out["no_split"]["stages_ms"]["sparse_attn"]
+    out["attn_speedup_from_split"] = round(n / a, 3)
+    return out
+
+
 def run_ours(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -257,6 +278,7 @@ def run_ours(args, rank, world):
         layer.q.mul_(args.logit_scale)          # exact for powers of two
     stream = torch.cuda.current_stream()
     flop = dense_equiv_flop(spec)
+    layer_splits = layer.kv_splits          # 1: no split-KV merge launch
 
     # --- warm-up and one index for the statistics ---
     for _ in range(args.warmup):
@@ -306,6 +328,8 @@ def run_ours(args, rank, world):
             measure_layer(layer8, spec8, min(args.steps, 5), 2, args.dense_steps, stream, fp8=True), spec8, 16.0,
             "e4m3")
         del layer8, case8
+        torch.cuda.empty_cache()
+        variants["bf16_chunk_512_at_128k"] = chunk_variant(dev, stream, min(args.steps, 5), args.dense_steps)
 
     peaks, peak_kind = load_peaks()
     attn_flop = stats["kept_flop"] + stats["corr_flop"]
@@ -334,7 +358,7 @@ def run_ours(args, rank, world):
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic(spec, args.logit_scale),
                      "kernel": "attn_kernel (fp_sparse_attn)",
                      "peak_source": f"{peak_kind} bf16 sustained (MEASURED_PEAKS.json)"},
-        "gpu_launches": 9 * args.steps,
+        "gpu_launches": (9 + (1 if layer_splits > 1 else 0)) * args.steps,
         "device_status": status,
         "clocks": clocks,
         "gen_seconds": round(gen_s, 1),

@@ -27,6 +27,7 @@ fp_status build_desc(const fp_problem *p, const fp_params *prm, BatchDesc *bd) {
     if (!p->cu_seqlens_q || !p->seqlens_k || !p->q_start_pos) return FP_ERR_INVALID;
     if (p->cu_seqlens_q[0] != 0) return FP_ERR_INVALID;
     if (prm->sink_tokens < 0 || prm->local_tokens < 0 || !(prm->alpha >= 0.f)) return FP_ERR_INVALID;
+    if (prm->kv_splits < 0 || prm->kv_splits > FP_MAX_KV_SPLITS) return FP_ERR_INVALID;
     memset(bd, 0, sizeof(*bd));
     bd->batch = p->batch;
     bd->h_q = p->h_q;
@@ -103,11 +104,48 @@ bool use_score_tc(const fp_problem *p, const BatchDesc &bd) {
     return score_tc_smem_bytes(bd.max_nkb) <= 227 * 1024;
 }
 
-size_t attn_ws_bytes(const BatchDesc &bd) {
-    size_t n = kWsHeaderBytes;
+// Split-KV parts per row.  Automatic: the persistent attention kernel runs
+// one CTA per SM (152 on a GB300) and takes units as SMs free up, so with U
+// units of about equal length, S parts per row finish in ceil(U*S/152)/S unit
+// times.  Take the S that minimises it (a larger S only when it gains >= 3%,
+// since every part adds a partial output to merge), with no part shorter
+// than ~16 terms; work lists of at least four units per SM are not split.
+int attn_splits(const BatchDesc &bd, const fp_params *prm) {
+    if (prm->kv_splits > 0) return prm->kv_splits;
+    constexpr long long kSm = 152;
+    const long long units = (long long)bd.total_rows * (bd.g / 2 > 0 ? bd.g / 2 : 1);
+    if (units <= 0 || units >= 4 * kSm) return 1;
+    const long long max_terms = bd.max_nkb + (bd.max_nkb + kBlock - 1) / kBlock;
+    long long cap = max_terms / 16;
+    cap = cap < FP_MAX_KV_SPLITS ? cap : FP_MAX_KV_SPLITS;
+    int best = 1;
+    double best_t = (double)((units + kSm - 1) / kSm);
+    for (long long s = 2; s <= cap; ++s) {
+        const double t = (double)((units * s + kSm - 1) / kSm) / (double)s;
+        if (t < 0.97 * best_t) {
+            best = (int)s;
+            best_t = t;
+        }
+    }
+    return best;
+}
+
+size_t attn_work_bytes(const BatchDesc &bd, int n_split) {
     // work schedule and, after it, the work-list cursor
-    n += align_up(((size_t)bd.total_rows * (bd.g / 2 > 0 ? bd.g / 2 : 1) + 1) * sizeof(int), 256);
+    return align_up(((size_t)bd.total_rows * (bd.g / 2 > 0 ? bd.g / 2 : 1) * n_split + 1) * sizeof(int), 256);
+}
+size_t attn_part_o_bytes(const BatchDesc &bd, int n_split) {
+    return n_split > 1 ? align_up((size_t)n_split * bd.total_q * bd.h_q * kHeadDim * sizeof(float), 256) : 0;
+}
+size_t attn_part_lse_bytes(const BatchDesc &bd, int n_split) {
+    return n_split > 1 ? align_up((size_t)n_split * bd.h_q * bd.total_q * sizeof(float), 256) : 0;
+}
+
+size_t attn_ws_bytes(const BatchDesc &bd, int n_split) {
+    size_t n = kWsHeaderBytes;
+    n += attn_work_bytes(bd, n_split);
     n += 2 * align_up((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2, 256);
+    n += attn_part_o_bytes(bd, n_split) + attn_part_lse_bytes(bd, n_split);
     return n;
 }
 
@@ -123,6 +161,7 @@ fp_params fp_default_params(void) {
     p.alpha = 0.1f;
     p.softmax_scale = 0.f;
     p.mean_correction = 1;
+    p.kv_splits = 0;
     return p;
 }
 
@@ -207,10 +246,16 @@ fp_status fp_select(const fp_problem *p, const fp_params *prm, const float *scor
     return FP_OK;
 }
 
+int fp_attn_kv_splits(const fp_problem *p, const fp_params *prm) {
+    BatchDesc bd;
+    if (build_desc(p, prm, &bd) != FP_OK) return -1;
+    return attn_splits(bd, prm);
+}
+
 size_t fp_attn_workspace_size(const fp_problem *p, const fp_params *prm) {
     BatchDesc bd;
     if (build_desc(p, prm, &bd) != FP_OK) return 0;
-    return attn_ws_bytes(bd);
+    return attn_ws_bytes(bd, attn_splits(bd, prm));
 }
 
 static fp_status run_attn(const fp_problem *p, const fp_params *prm, const int *row_ptr, const int *col_idx,
@@ -222,7 +267,8 @@ static fp_status run_attn(const fp_problem *p, const fp_params *prm, const int *
     if ((s = check_kv(p, bd)) != FP_OK || (s = check_q(p)) != FP_OK) return s;
     if (bd.g % 2) return FP_ERR_UNSUPPORTED;
     if (!out || !aligned16(out)) return FP_ERR_INVALID;
-    if (!ws || ws_bytes < attn_ws_bytes(bd)) return FP_ERR_WORKSPACE;
+    const int n_split = attn_splits(bd, prm);
+    if (!ws || ws_bytes < attn_ws_bytes(bd, n_split)) return FP_ERR_WORKSPACE;
     char *w = static_cast<char *>(ws);
     AttnLaunch L;
     memset(&L, 0, sizeof(L));
@@ -247,10 +293,15 @@ static fp_status run_attn(const fp_problem *p, const fp_params *prm, const int *
     L.status = status_ptr(ws);
     size_t off = kWsHeaderBytes;
     L.work = reinterpret_cast<int *>(w + off);
-    off += align_up(((size_t)bd.total_rows * (bd.g / 2 > 0 ? bd.g / 2 : 1) + 1) * sizeof(int), 256);
+    off += attn_work_bytes(bd, n_split);
     L.km16 = reinterpret_cast<__nv_bfloat16 *>(w + off);
     off += align_up((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2, 256);
     L.vm16 = reinterpret_cast<__nv_bfloat16 *>(w + off);
+    off += align_up((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2, 256);
+    L.n_split = n_split;
+    L.part_o = n_split > 1 ? reinterpret_cast<float *>(w + off) : nullptr;
+    off += attn_part_o_bytes(bd, n_split);
+    L.part_lse = n_split > 1 ? reinterpret_cast<float *>(w + off) : nullptr;
     L.wait_ns = g_wait_ns;
     L.fp8 = p->dtype == FP_E4M3;
     L.q_scale = p->q_scale;

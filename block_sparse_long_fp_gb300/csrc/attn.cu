@@ -35,6 +35,8 @@
 #include <stdio.h>
 #include <stdlib.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "sm100.cuh"
 #include "launch.cuh"
@@ -70,8 +72,11 @@ constexpr int kMetaConsumers = 10;
 struct UnitMeta {
     int pos;                          // position in the work list; -1: no more units
     int unit;                         // unit id
-    int n_items;                      // kept blocks + mean tiles
-    int n_corr;                       // mean tiles
+    int n_items;                      // terms of this unit's part (kept blocks, then mean tiles)
+    int n_corr;                       // mean tiles of the whole row
+    int jb;                           // the part's first term in the row's list
+    int n_kept;                       // kept blocks of the row (terms before the mean tiles)
+    int pad[2];
     uint32_t bitmap[kBitmapWords];    // kept blocks J < I
     int corr[kMaxCorrTiles];          // mean tiles holding a skipped block
 };
@@ -92,7 +97,11 @@ struct AttnArgs {
     int page_size;
     int num_pages;
     int n_pairs;              // query-head pairs per kv head
+    int n_split;              // split-KV parts per row (1: none)
+    float *part_o;            // n_split > 1: fp32 partial outputs [n_split, total_q, h_q, d]
+    float *part_lse;          // n_split > 1: partial LSEs [n_split, h_q, total_q]
     int mean_corr;
+    int mean_rows;            // e4m3: row offset of the lo term of the key means
     float scale_log2;         // softmax scale * log2(e)
     const float *q_scale;     // e4m3 only: per query head / kv head scales
     const float *k_scale;
@@ -112,13 +121,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // one work unit: index row (request r, query block I, kv head h) and a pair of
 // query heads hq0, hq0 + 1 of the group
 struct Unit {
-    int row, r, il, h, I, hq0, rp0, n_kept;
+    int row, r, il, h, I, hq0, rp0, n_kept, split;
 };
 
+// unit id = (row * n_pairs + pair) * n_split + part
 __device__ __forceinline__ Unit decode_unit(const BatchDesc &bd, const AttnArgs &a, int unit) {
     Unit U;
-    U.row = unit / a.n_pairs;
-    const int pair = unit % a.n_pairs;
+    U.split = unit % a.n_split;
+    const int rp = unit / a.n_split;
+    U.row = rp / a.n_pairs;
+    const int pair = rp % a.n_pairs;
     U.r = req_of_row(bd, U.row);
     const ReqDesc &rq = bd.req[U.r];
     const int local = U.row - rq.row_base;
@@ -142,7 +154,10 @@ __device__ __forceinline__ Unit decode_unit(const BatchDesc &bd, const AttnArgs 
 // items (K/V ring slots, S and P handshakes), `kq` its non-empty units (Q and
 // O handshakes), `k` all its units (metadata buffers).  The next unit's Q,
 // K and V loads and its first S MMAs overlap the current unit's epilogue.
-template <bool kFp8>
+// kLse (e4m3 only): also keep the sum of the unrounded weights, for an LSE
+// that counts the weights e4m3 flushes (wanted when the caller asks for the
+// LSE or rows are split; it costs ~10% of the e4m3 kernel)
+template <bool kFp8, bool kLse>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtensorMap tmQ,
             const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -208,11 +223,12 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 if (lane == 0) pos = atomicAdd(a.next_unit, 1);
                 pos = __shfl_sync(0xffffffffu, pos, 0);
                 const bool end = pos >= a.n_units;
-                int unit = 0, n_corr = 0, n_kept = 0;
+                int unit = 0, n_corr = 0, n_kept = 0, split = 0;
                 if (!end) {
                     unit = __ldg(a.work + pos);
                     const Unit U = decode_unit(bd, a, unit);
                     n_kept = U.n_kept;
+                    split = U.split;
                     const int I = U.I;
                     if (sparse && a.mean_corr && I > 0) {
                         const int nw = (I + 31) / 32;
@@ -242,10 +258,16 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     }
                 }
                 if (lane == 0) {
+                    // this part's share of the row's terms
+                    const int n_terms = n_kept + n_corr;
+                    const int jb = (int)((long long)split * n_terms / a.n_split);
+                    const int je = (int)((long long)(split + 1) * n_terms / a.n_split);
                     M.pos = end ? -1 : pos;
                     M.unit = unit;
-                    M.n_items = n_kept + n_corr;
+                    M.n_items = je - jb;
                     M.n_corr = n_corr;
+                    M.jb = jb;
+                    M.n_kept = n_kept;
                 }
                 __syncwarp();
                 mbar_arrive(bar(BAR_MF + b));
@@ -321,11 +343,14 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         }
                     }
                     if (!__shfl_sync(0xffffffffu, good, 0)) break;
+                    // terms jb .. jb + n_items - 1 of the row (this unit's part)
+                    const int jb = M.jb;
                     int pg_n, off_n;
-                    look(0, pg_n, off_n);
+                    look(jb, pg_n, off_n);
                     int z_cur = oob;
-                    for (int j = 0; j < n_items && good; ++j, ++it) {
-                        const int lj = j % per;
+                    for (int jl = 0; jl < n_items && good; ++jl, ++it) {
+                        const int j = jb + jl;
+                        const int lj = jl % per;
                         if (lj == 0) {                      // next round: take it, look up the one after
                             z_cur = row_of(pg_n, off_n);
                             look(j + per, pg_n, off_n);
@@ -346,7 +371,9 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                                     break;
                                 }
                                 const uint32_t dst = sbase + (op == 0 ? kSmemK : kSmemV) + s * kTileBytes;
-                                mbar_expect_tx(full, kT);
+                                // e4m3 mean K tiles carry a second (lo) term in the slot's upper half
+                                const bool two = kFp8 && !kept && op == 0;
+                                mbar_expect_tx(full, two ? 2 * kT : kT);
                                 if (kept) {
                                     const CUtensorMap *tm = op == 0 ? &tmK : &tmV;
 #pragma unroll
@@ -359,6 +386,8 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                                     const CUtensorMap *tm = op == 0 ? &tmKm : &tmVm;
                                     for (int hf = 0; hf < kNH; ++hf)
                                         tma_load_3d(dst + hf * kHalfBytes, tm, full, hf * 64, U.h, rq.kb_base + c * kBlock);
+                                    if (two)
+                                        tma_load_3d(dst + kHalfBytes, tm, full, 0, U.h, a.mean_rows + rq.kb_base + c * kBlock);
                                 }
                             }
                         }
@@ -380,7 +409,9 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             const uint64_t qdesc = smem_desc_sw128(sbase + kSmemQ, 16, 1024);
             const uint64_t kdesc = smem_desc_sw128(sbase + kSmemK, 16, 1024);
             const uint64_t vdesc = smem_desc_sw128(sbase + kSmemV, kFp8 ? 16 : kHalfBytes, 1024);
-            auto issue_S = [&](int t, int s) {
+            // two: an e4m3 mean tile, whose keys come as hi + lo terms (the lo
+            // tile sits in the upper half of the slot)
+            auto issue_S = [&](int t, int s, bool two) {
                 const uint64_t qd = qdesc + ((t * kTileBytes) >> 4);
                 const uint64_t kd = kdesc + ((s * kTileBytes) >> 4);
 #pragma unroll
@@ -388,6 +419,13 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     const uint32_t off = (kFp8 ? kk * 32 : (kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
                     if constexpr (kFp8) mma_ss_f8(tmem + t * 256, qd + off, kd + off, idS, kk > 0);
                     else mma_ss(tmem + t * 256, qd + off, kd + off, idS, kk > 0);
+                }
+                if constexpr (kFp8) {
+                    if (two) {
+#pragma unroll 1
+                        for (int kk = 0; kk < kKSteps; ++kk)
+                            mma_ss_f8(tmem + t * 256, qd + kk * 2, kd + (kHalfBytes >> 4) + kk * 2, idS, true);
+                    }
                 }
             };
             auto issue_PV = [&](int t, int s, bool acc) {
@@ -405,15 +443,16 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 const int b = k & 1;
                 if (!mbar_wait(bar(BAR_MF + b), (k >> 1) & 1, abort_flag, a.status, a.wait_ns)) break;
                 const int pos = meta[b].pos, n_items = meta[b].n_items;
+                const int first_mean = meta[b].n_kept - meta[b].jb;   // local index of the first mean tile
                 mbar_arrive(bar(BAR_ME + b));
                 if (pos < 0) break;
                 if (n_items == 0) continue;
                 if (!mbar_wait(bar(BAR_Q), kq & 1, abort_flag, a.status, a.wait_ns)) break;
                 if (!mbar_wait(bar(BAR_KF + (it & 1)), (it >> 1) & 1, abort_flag, a.status, a.wait_ns)) break;
                 tc_fence_after();
-                issue_S(0, it & 1);
+                issue_S(0, it & 1, first_mean <= 0);
                 tc_commit(bar(BAR_SF + 0));
-                issue_S(1, it & 1);
+                issue_S(1, it & 1, first_mean <= 0);
                 tc_commit(bar(BAR_SF + 1));
                 tc_commit(bar(BAR_KE + (it & 1)));
                 if (n_items == 1) tc_commit(bar(BAR_QE));
@@ -435,7 +474,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                             break;
                         }
                         tc_fence_after();
-                        issue_S(0, s1);
+                        issue_S(0, s1, j + 1 >= first_mean);
                         tc_commit(bar(BAR_SF + 0));
                     } else {
                         tc_commit(bar(BAR_OF + 0));
@@ -448,7 +487,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     issue_PV(1, s, j > 0);
                     tc_commit(bar(BAR_VE + s));
                     if (more) {
-                        issue_S(1, s1);
+                        issue_S(1, s1, j + 1 >= first_mean);
                         tc_commit(bar(BAR_SF + 1));
                         tc_commit(bar(BAR_KE + s1));
                         if (j + 2 == n_items) tc_commit(bar(BAR_QE));   // the unit's last S MMAs
@@ -484,18 +523,30 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             const int qi = U.il * kBlock + rowt;          // query index inside the request
             const int head = U.hq0 + t;
             if (n_items == 0) {
-                // a row with no term at all: O = 0, LSE = -inf
+                // a row (or part) with no term at all: O = 0, LSE = -inf
                 if (qi < rq.lq) {
-                    __nv_bfloat16 *dst = a.out + ((long long)(rq.q_off + qi) * bd.h_q + head) * kHeadDim;
-                    for (int c = 0; c < kHeadDim; c += 8) *reinterpret_cast<uint4 *>(dst + c) = make_uint4(0, 0, 0, 0);
-                    if (a.lse) a.lse[(long long)head * bd.total_q + rq.q_off + qi] = -INFINITY;
+                    const long long tok = rq.q_off + qi;
+                    if (a.n_split > 1) {
+                        float *pdst = a.part_o + (((long long)U.split * bd.total_q + tok) * bd.h_q + head) * kHeadDim;
+                        for (int c = 0; c < kHeadDim; c += 4) *reinterpret_cast<float4 *>(pdst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+                        a.part_lse[((long long)U.split * bd.h_q + head) * bd.total_q + tok] = -INFINITY;
+                    } else {
+                        __nv_bfloat16 *dst = a.out + (tok * bd.h_q + head) * kHeadDim;
+                        for (int c = 0; c < kHeadDim; c += 8) *reinterpret_cast<uint4 *>(dst + c) = make_uint4(0, 0, 0, 0);
+                        if (a.lse) a.lse[(long long)head * bd.total_q + tok] = -INFINITY;
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(BAR_ME + b));
                 continue;
             }
             const int pos = rq.start + qi;                // absolute position
-            float m = -INFINITY, l = 0.f;
+            // l: sum of the weights the MMA multiplies (normalises O); e4m3 also
+            // keeps lt, the sum of the unrounded weights, for the LSE: weights
+            // below e4m3's range (a long row's tail) flush to zero in P, and the
+            // LSE (which split-KV merges by) must still count them
+            float m = -INFINITY, l = 0.f, lt = 0.f;
+
             const int last_J = n_kept == 0 ? -1 : (sparse ? __ldg(a.col_idx + U.rp0 + n_kept - 1) : n_kept - 1);
             bool ok = true;
             // logit scale (log2 units): e4m3 codes carry the per-head scales
@@ -505,7 +556,9 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             // the largest weight of a row is exactly 256 = e4m3(256 * 1) and only
             // the smaller weights carry e4m3 rounding.
             constexpr float kTau = kFp8 ? 0.f : 8.f;
-            for (int j = 0; j < n_items; ++j, ++it) {
+            const int jb = M.jb;                          // this unit's part: terms jb ..
+            for (int jl = 0; jl < n_items; ++jl, ++it) {
+                const int j = jb + jl;
                 const bool got = mbar_wait(bar(BAR_SF + t), it & 1, abort_flag, a.status, a.wait_ns);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }   // tcgen05.ld needs the whole warp
                 tc_fence_after();
@@ -565,6 +618,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 const float f = grow ? fast_exp2(m - mx) : 1.f;   // 0 when m = -inf
                 if (grow) {
                     l *= f;
+                    if constexpr (kFp8 && kLse) lt *= f;
                     m = mx;
                 }
                 const float off = bias - (m == -INFINITY ? 0.f : m);
@@ -587,22 +641,38 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         tmem_st32(tS + 32 * half, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * half));
                     }
                 } else {
-                    // e4m3 of 256 * p: four weights per TMEM column
+                    // e4m3 of 256 * p: four weights per TMEM column (and, with
+                    // kLse, the sum of the unrounded weights)
                     const uint64_t oo = f2_pack(off + 8.f, off + 8.f);
+                    auto exps = [&](auto with_sum) {
+                        uint64_t ltp[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float z0, z1, z2, z3;
-                        f2_unpack(f2_fma(f2_pack(x[4 * e], x[4 * e + 1]), cc, oo), z0, z1);
-                        f2_unpack(f2_fma(f2_pack(x[4 * e + 2], x[4 * e + 3]), cc, oo), z2, z3);
-                        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                            make_float2(fast_exp2(z0), fast_exp2(z1)), __NV_SATFINITE, __NV_E4M3);
-                        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                            make_float2(fast_exp2(z2), fast_exp2(z3)), __NV_SATFINITE, __NV_E4M3);
-                        pk[e] = (uint32_t)lo | ((uint32_t)hi << 16);
-                    }
-                    tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+                        for (int e = 0; e < 32; ++e) {
+                            float z0, z1, z2, z3;
+                            f2_unpack(f2_fma(f2_pack(x[4 * e], x[4 * e + 1]), cc, oo), z0, z1);
+                            f2_unpack(f2_fma(f2_pack(x[4 * e + 2], x[4 * e + 3]), cc, oo), z2, z3);
+                            const float p0 = fast_exp2(z0), p1 = fast_exp2(z1), p2 = fast_exp2(z2), p3 = fast_exp2(z3);
+                            if constexpr (decltype(with_sum)::value) {
+                                ltp[0] = f2_add(ltp[0], f2_pack(p0, p1));
+                                ltp[1] = f2_add(ltp[1], f2_pack(p2, p3));
+                            }
+                            const __nv_fp8x2_storage_t lo =
+                                __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
+                            const __nv_fp8x2_storage_t hi =
+                                __nv_cvt_float2_to_fp8x2(make_float2(p2, p3), __NV_SATFINITE, __NV_E4M3);
+                            pk[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+                        }
+                        tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+                        if constexpr (decltype(with_sum)::value) {
+                            float t0, t1, t2, t3;
+                            f2_unpack(ltp[0], t0, t1);
+                            f2_unpack(ltp[1], t2, t3);
+                            lt += (t0 + t1) + (t2 + t3);
+                        }
+                    };
+                    exps(std::integral_constant<bool, kLse>{});
                 }
-                if (any_grow && j > 0) {
+                if (any_grow && jl > 0) {
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         uint32_t o[32];
@@ -665,14 +735,17 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             // O = (sum of weights * v codes) * v_scale / (sum of weights); for e4m3
             // both sums carry the factor 256, which cancels
             const float inv = l > 0.f ? (kFp8 ? __ldg(a.v_scale + V.h) : 1.f) / l : 0.f;
-            __nv_bfloat16 *dst = a.out + ((long long)(rv.q_off + qv) * bd.h_q + hv) * kHeadDim;
+            const long long tok = rv.q_off + qv;
+            const bool part = a.n_split > 1;            // split-KV: fp32 partial O of this part
+            __nv_bfloat16 *dst = a.out + (tok * bd.h_q + hv) * kHeadDim;
+            float *pdst = part ? a.part_o + (((long long)V.split * bd.total_q + tok) * bd.h_q + hv) * kHeadDim : nullptr;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
                 tmem_ld32(tO + c * 32, o);
                 tmem_ld_wait();
                 reg_fence(o);
-                if (valid) {
+                if (valid && !part) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
                         uint4 w;
@@ -682,14 +755,22 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         w.w = pack_bf16(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
                         *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
                     }
+                } else if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(pdst + c * 32 + e) =
+                            make_float4(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv,
+                                        __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
                 }
             }
             // the next unit's first PV MMA overwrites O only after this warp
             // group's next P handshake, which follows these reads
             tc_fence_before();
-            if (valid && a.lse)
-                a.lse[(long long)hv * bd.total_q + rv.q_off + qv] =
-                    l > 0.f ? (m + __log2f(l) - (kFp8 ? 8.f : 0.f)) * 0.6931471805599453f : -INFINITY;
+            const float lsum = kFp8 && kLse ? lt : l;
+            const float lse_v =
+                l > 0.f ? (m + __log2f(lsum) - (kFp8 ? 8.f : 0.f)) * 0.6931471805599453f : -INFINITY;
+            if (valid && part) a.part_lse[((long long)V.split * bd.h_q + hv) * bd.total_q + tok] = lse_v;
+            else if (valid && a.lse) a.lse[(long long)hv * bd.total_q + tok] = lse_v;
             ++kq;
         }
     }
@@ -715,8 +796,8 @@ constexpr int kSchedBins = 4096;
 constexpr int kSchedThreads = 1024;
 
 __global__ void __launch_bounds__(kSchedThreads)
-sched_kernel(const __grid_constant__ BatchDesc bd, const int *__restrict__ row_ptr, int n_pairs, int mean_corr,
-             int *__restrict__ work, int *__restrict__ next_unit) {
+sched_kernel(const __grid_constant__ BatchDesc bd, const int *__restrict__ row_ptr, int n_pairs, int n_split,
+             int mean_corr, int *__restrict__ work, int *__restrict__ next_unit) {
     __shared__ int hist[kSchedBins];
     __shared__ int warp_sum[kSchedThreads / 32];
     __shared__ int grp[3];                          // request, kv head, first position of the group
@@ -734,11 +815,12 @@ sched_kernel(const __grid_constant__ BatchDesc bd, const int *__restrict__ row_p
         }
         const int rank = blockIdx.x / bd.h_kv, h = blockIdx.x % bd.h_kv;
         int base = 0;
-        for (int k = 0; k < rank; ++k) base += bd.req[ord[k]].nqb * bd.h_kv * n_pairs;
+        const int per_row = n_pairs * n_split;          // units of one index row
+        for (int k = 0; k < rank; ++k) base += bd.req[ord[k]].nqb * bd.h_kv * per_row;
         const int r = ord[rank];
         grp[0] = r;
         grp[1] = h;
-        grp[2] = base + h * bd.req[r].nqb * n_pairs;
+        grp[2] = base + h * bd.req[r].nqb * per_row;
     }
     for (int k = tid; k < kSchedBins; k += kSchedThreads) hist[k] = 0;
     __syncthreads();
@@ -788,8 +870,43 @@ sched_kernel(const __grid_constant__ BatchDesc bd, const int *__restrict__ row_p
     for (int il = tid; il < rq.nqb; il += kSchedThreads) {
         const int slot = atomicAdd(&hist[cost(il)], 1);
         const int row = rq.row_base + il * bd.h_kv + h;
-        for (int p = 0; p < n_pairs; ++p) work[base + slot * n_pairs + p] = row * n_pairs + p;
+        const int per_row = n_pairs * n_split;
+        for (int u = 0; u < per_row; ++u) work[base + slot * per_row + u] = row * per_row + u;
     }
+}
+
+// split-KV merge: O = sum_s e^{LSE_s - LSE} O_s, LSE = ln sum_s e^{LSE_s}, one warp
+// per (query, head), four values of d per lane
+__global__ void __launch_bounds__(256)
+combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse, int n_split, long long total_q,
+               int h_q, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse) {
+    const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+    const int lane = threadIdx.x % 32;
+    if (w >= total_q * h_q) return;
+    const long long tok = w / h_q;
+    const int head = (int)(w % h_q);
+    float mx = -INFINITY;
+    for (int s = 0; s < n_split; ++s) mx = fmaxf(mx, __ldg(part_lse + ((long long)s * h_q + head) * total_q + tok));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+    if (mx != -INFINITY) {
+        for (int s = 0; s < n_split; ++s) {
+            const float ls = __ldg(part_lse + ((long long)s * h_q + head) * total_q + tok);
+            const float wgt = ls == -INFINITY ? 0.f : __expf(ls - mx);
+            den += wgt;
+            const float4 o = __ldg(reinterpret_cast<const float4 *>(part_o + (((long long)s * total_q + tok) * h_q + head) * kHeadDim) + lane);
+            acc.x = fmaf(wgt, o.x, acc.x);
+            acc.y = fmaf(wgt, o.y, acc.y);
+            acc.z = fmaf(wgt, o.z, acc.z);
+            acc.w = fmaf(wgt, o.w, acc.w);
+        }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    uint2 pk;
+    pk.x = pack_bf16(acc.x * inv, acc.y * inv);
+    pk.y = pack_bf16(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2 *>(out + (tok * h_q + head) * kHeadDim + 4 * lane) = pk;
+    if (lse && lane == 0) lse[(long long)head * total_q + tok] = den > 0.f ? mx + __logf(den) : -INFINITY;
 }
 
 // fp32 block means -> bf16 operands of the mean tiles; [n, n_pad) is zeroed
@@ -805,7 +922,12 @@ __global__ void to_bf16_kernel(const float *__restrict__ a, const float *__restr
 
 
 // fp32 block means -> e4m3 codes with the per-head K / V scales (block means
-// never exceed the largest |value| the scale maps to 448); [n, n_pad) is zeroed
+// never exceed the largest |value| the scale maps to 448); [n, n_pad) is zeroed.
+// The key means get two terms, hi at ao[k] and lo = e4m3(x - hi) at
+// ao[n_pad + k] (about 8 significant bits together): a mean token's logit
+// enters the exponent, and one e4m3 term (2^-4 relative) moved the LSE of
+// long sharp rows by ~0.1.  The value means keep one term (they enter O
+// linearly).
 __global__ void to_e4m3_kernel(const float *__restrict__ a, const float *__restrict__ b, const float *__restrict__ sa,
                                const float *__restrict__ sb, uint8_t *__restrict__ ao, uint8_t *__restrict__ bo,
                                long long n, long long n_pad, int h_kv) {
@@ -815,7 +937,11 @@ __global__ void to_e4m3_kernel(const float *__restrict__ a, const float *__restr
         const float ia = 1.f / __ldg(sa + h), ib = 1.f / __ldg(sb + h);
         const float2 va = k < n ? make_float2(a[k] * ia, a[k + 1] * ia) : make_float2(0.f, 0.f);
         const float2 vb = k < n ? make_float2(b[k] * ib, b[k + 1] * ib) : make_float2(0.f, 0.f);
-        *reinterpret_cast<__nv_fp8x2_storage_t *>(ao + k) = __nv_cvt_float2_to_fp8x2(va, __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(va, __NV_SATFINITE, __NV_E4M3);
+        const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
+        *reinterpret_cast<__nv_fp8x2_storage_t *>(ao + k) = hi;
+        *reinterpret_cast<__nv_fp8x2_storage_t *>(ao + n_pad + k) =
+            __nv_cvt_float2_to_fp8x2(make_float2(va.x - hf.x, va.y - hf.y), __NV_SATFINITE, __NV_E4M3);
         *reinterpret_cast<__nv_fp8x2_storage_t *>(bo + k) = __nv_cvt_float2_to_fp8x2(vb, __NV_SATFINITE, __NV_E4M3);
     }
 }
@@ -882,7 +1008,8 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     const BatchDesc &bd = *L.bd;
     const int n_pairs = bd.g / 2;
     const bool sparse = L.row_ptr != nullptr;
-    const int units = bd.total_rows * n_pairs;
+    const int n_split = L.n_split > 1 ? L.n_split : 1;
+    const int units = bd.total_rows * n_pairs * n_split;
     if (units == 0) return FP_OK;
     const int rpb = L.page_size < kBlock ? L.page_size : kBlock;
     CUtensorMap tmQ, tmK, tmV, tmKm, tmVm;
@@ -906,7 +1033,9 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
         else
             to_bf16_kernel<<<1024, 256, 0, st>>>(L.k_mean, L.v_mean, L.km16, L.vm16, n, n_pad);
         if ((e = cudaGetLastError()) != cudaSuccess) return fail("mean conversion launch", (int)e);
-        if (!make_map(&tmKm, L.km16, bd.h_kv, mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock, f8))
+        // e4m3: hi rows [0, mean_rows), lo rows [mean_rows, 2 mean_rows)
+        if (!make_map(&tmKm, L.km16, bd.h_kv, (f8 ? 2LL : 1LL) * mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim,
+                      kBlock, f8))
             return fail("mean K map", 0);
         if (!make_map(&tmVm, L.vm16, bd.h_kv, mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock, f8))
             return fail("mean V map", 0);
@@ -915,8 +1044,8 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
         tmVm = tmV;
     }
     int *next_unit = L.work + units;
-    sched_kernel<<<bd.batch * bd.h_kv, kSchedThreads, 0, st>>>(bd, L.row_ptr, n_pairs, use_means ? 1 : 0, L.work,
-                                                              next_unit);
+    sched_kernel<<<bd.batch * bd.h_kv, kSchedThreads, 0, st>>>(bd, L.row_ptr, n_pairs, n_split, use_means ? 1 : 0,
+                                                              L.work, next_unit);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail("schedule launch", (int)e);
     AttnArgs a;
     a.row_ptr = L.row_ptr;
@@ -929,7 +1058,11 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     a.page_size = L.page_size;
     a.num_pages = L.num_pages;
     a.n_pairs = n_pairs;
+    a.n_split = n_split;
+    a.part_o = L.part_o;
+    a.part_lse = L.part_lse;
     a.mean_corr = use_means ? 1 : 0;
+    a.mean_rows = mean_rows(bd);
     a.scale_log2 = L.softmax_scale * 1.4426950408889634f;
     a.q_scale = L.q_scale;
     a.k_scale = L.k_scale;
@@ -938,7 +1071,8 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     a.lse = L.lse;
     a.status = L.status;
     a.wait_ns = L.wait_ns;
-    auto kern = f8 ? attn_kernel<true> : attn_kernel<false>;
+    const bool want_lse = L.lse != nullptr || n_split > 1;
+    auto kern = f8 ? (want_lse ? attn_kernel<true, true> : attn_kernel<true, false>) : attn_kernel<false, false>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttn)) != cudaSuccess)
         return fail("attention smem attribute", (int)e);
     // persistent: one CTA per SM (the shared memory admits one), never more than units
@@ -951,6 +1085,13 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     if ((e = cudaGetLastError()) != cudaSuccess) {
         if (debug_on()) fprintf(stderr, "[fprefill] attention launch: %s\n", cudaGetErrorString(e));
         return fail("attention launch", (int)e);
+    }
+    if (n_split > 1) {
+        const long long warps = (long long)bd.total_q * bd.h_q;
+        const long long blocks = (warps * 32 + 255) / 256;
+        combine_kernel<<<(unsigned)blocks, 256, 0, st>>>(L.part_o, L.part_lse, n_split, bd.total_q, bd.h_q,
+                                                         (__nv_bfloat16 *)L.out, L.lse);
+        if ((e = cudaGetLastError()) != cudaSuccess) return fail("split-KV merge launch", (int)e);
     }
     return FP_OK;
 }

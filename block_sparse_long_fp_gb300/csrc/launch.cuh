@@ -46,6 +46,9 @@ struct AttnLaunch {
     unsigned long long wait_ns;
     bool fp8;                         // e4m3 q / k / v with per-head scales
     const float *q_scale, *k_scale, *v_scale;
+    int n_split;                      // split-KV parts per row (1: none)
+    float *part_o;                    // [n_split, total_q, h_q, d] fp32 when n_split > 1
+    float *part_lse;                  // [n_split, h_q, total_q] fp32 when n_split > 1
 };
 int launch_attn(const AttnLaunch &L, cudaStream_t st);
 // rows of the bf16 block-mean copies: at least one full 128-row TMA box

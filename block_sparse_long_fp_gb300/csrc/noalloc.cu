@@ -53,6 +53,14 @@ fp_status scratch_on_current_device(void **addr) {
 extern "C" fp_status fp_sparse_attn_noalloc(const fp_problem *p, const fp_params *prm, const int *row_ptr,
                                             const int *col_idx, const float *k_mean, const float *v_mean,
                                             void *out, float *lse_opt, int *status_dev_opt, void *stream) {
+    // The fixed scratch does not split rows unless the caller asks for it
+    // (kv_splits 0 means 1 here): split-KV partial outputs would crowd it.
+    fp_params q;
+    if (prm) {
+        q = *prm;
+        if (q.kv_splits == 0) q.kv_splits = 1;
+        prm = &q;
+    }
     // Argument checks first, with no workspace: every argument error comes back
     // as from fp_sparse_attn; FP_ERR_WORKSPACE means the arguments are fine.
     fp_status s = fp_sparse_attn(p, prm, row_ptr, col_idx, k_mean, v_mean, out, lse_opt, nullptr, 0, stream);

@@ -23,7 +23,8 @@ FP_MAX_BATCH = 128
 
 class FpParams(Structure):
     _fields_ = [("block", c_int), ("sink_tokens", c_int), ("local_tokens", c_int),
-                ("alpha", c_float), ("softmax_scale", c_float), ("mean_correction", c_int)]
+                ("alpha", c_float), ("softmax_scale", c_float), ("mean_correction", c_int),
+                ("kv_splits", c_int)]
 
 
 class FpProblem(Structure):
@@ -65,6 +66,7 @@ def lib():
             "fp_select": ([P, PP, c_void_p, c_void_p, c_void_p, c_longlong, c_void_p, c_void_p,
                            c_void_p, c_size_t, c_void_p], c_int),
             "fp_attn_workspace_size": ([P, PP], c_size_t),
+            "fp_attn_kv_splits": ([P, PP], c_int),
             "fp_sparse_attn": ([P, PP, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                 c_void_p, c_size_t, c_void_p], c_int),
             "fp_dense_attn": ([P, PP, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
@@ -153,6 +155,7 @@ class Layer:
         self.key_blocks = int(L.fp_num_key_blocks(pp, pm))
         self.score_size = int(L.fp_score_size(pp, pm))
         self.total_q = int(L.fp_total_q(pp))
+        self.kv_splits = int(L.fp_attn_kv_splits(pp, pm))   # split-KV parts of the attention calls
         self.ws_bytes = max(int(L.fp_discover_workspace_size(pp, pm)),
                             int(L.fp_select_workspace_size(pp, pm)),
                             int(L.fp_attn_workspace_size(pp, pm)))

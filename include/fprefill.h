@@ -95,7 +95,13 @@ typedef struct {
     float alpha;          /* keep J when Score[I,J] >= alpha * max_J Score[I,J] (0.1) */
     float softmax_scale;  /* logit scale; <= 0 selects 1/sqrt(d) */
     int mean_correction;  /* 1: skipped blocks J < I add their block-mean term */
+    int kv_splits;        /* attention only: split each row's key list into this many
+                             parts merged by their LSE (split-KV); 0 chooses (more
+                             parts when the problem has too few work units to fill
+                             the GPU), 1 never splits; at most FP_MAX_KV_SPLITS */
 } fp_params;
+
+#define FP_MAX_KV_SPLITS 32
 
 typedef struct {
     int batch;
@@ -123,7 +129,8 @@ typedef struct {
 } fp_problem;
 
 /* Defaults of the pages: B=128, sink 256, local 512, alpha 0.1, 1/sqrt(d),
- * mean correction on [V2 paper reading, section 4 configuration]. */
+ * mean correction on [V2 paper reading, section 4 configuration]; kv_splits 0
+ * (chosen by the library). */
 fp_params fp_default_params(void);
 
 /* Sizes derived from the host descriptors (element counts, not bytes). */
@@ -183,10 +190,21 @@ fp_status fp_select(const fp_problem *p, const fp_params *prm, const float *scor
  *   out (device bf16 [total_q, h_q, d], contiguous).
  *   lse_opt (device fp32 [h_q, total_q], natural log; may be NULL).
  *   ws: fp_attn_workspace_size() bytes (work schedule, bf16 copies of the
- *   block means).
+ *   block means, and with split-KV the fp32 partial outputs and LSEs).
  * A row with no term at all (an empty index row, no correction) yields O = 0.
+ *
+ * Split-KV (the kept-count load balancing of the V2 popular article, "KV
+ * split", for rows too long for the number of rows): with S = the split count
+ * chosen from params.kv_splits, each row's terms (kept blocks, then mean
+ * tiles) are cut into S consecutive parts of equal size.  Part s yields
+ * O_s, LSE_s over its own terms, and O = sum_s e^{LSE_s - LSE} O_s with
+ * LSE = ln sum_s e^{LSE_s}: the same O up to rounding.  The workspace size
+ * depends on the split count, so query it with the same params.
  * ------------------------------------------------------------------------- */
 size_t fp_attn_workspace_size(const fp_problem *p, const fp_params *prm);
+/* The split count S the attention calls use for these params (>= 1), or -1
+ * on an argument error. */
+int fp_attn_kv_splits(const fp_problem *p, const fp_params *prm);
 fp_status fp_sparse_attn(const fp_problem *p, const fp_params *prm, const int *row_ptr,
                          const int *col_idx, const float *k_mean, const float *v_mean,
                          void *out, float *lse_opt, void *ws, size_t ws_bytes, void *stream);
@@ -203,7 +221,8 @@ fp_status fp_sparse_attn(const fp_problem *p, const fp_params *prm, const int *r
  * that loads the library until the process exits.  The caller still provides
  * the inputs and the outputs.
  *
- *   Arguments and results as fp_sparse_attn, without ws / ws_bytes.
+ *   Arguments and results as fp_sparse_attn, without ws / ws_bytes; rows are
+ *   split only when params.kv_splits asks for it (0 means no split here).
  *   status_dev_opt (device int32 [1], may be NULL): receives this call's
  *     device status word (FP_OK or an fp_status code), in stream order after
  *     the kernels -- the scratch itself is not visible to the caller.

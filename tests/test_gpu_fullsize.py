@@ -73,8 +73,10 @@ def sampled_parity(spec, alpha=0.1, mean_corr=True, rows_per_request=3, queries_
             assert not np.any((kept != keep_ref) & ~flag), (r, i, h)
             kept_total += int(keep_ref.sum())
             causal_total += I + 1
+            # the attention on the blocks the GPU kept (they equal the oracle's
+            # outside the flagged near-threshold band, checked just above)
             keep = np.zeros((1, hkv, nkb), np.uint8)
-            keep[0, h, :I + 1] = keep_ref
+            keep[0, h, :I + 1] = kept
             nrow = q1 - q0
             qi = rng.integers(0, nrow, queries_per_row)
             qi[0] = nrow - 1
