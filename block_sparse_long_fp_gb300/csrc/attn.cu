@@ -2,8 +2,8 @@
 //
 // What it computes: the sparse attention of the FlashPrefill V2 paper reading,
 // section 4.1 -- kept key blocks exactly, every skipped earlier block J < I as
-// one "mean token" (kmean_J, vmean_J) of weight n_J (the V2 popular article:
-// "multiplied by the number of tokens the block originally had") -- over a
+// one mean token (kmean_J, vmean_J) of weight n_J (the V2 popular article,
+// mean-correction section: the block's token count) -- over a
 // paged KV cache (V2 section 4.3: the address of a key is the page-table entry
 // of its page plus its offset in the page, fetched asynchronously), with the
 // g query heads of a kv group packed so that each kept KV tile is fetched once
