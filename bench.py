@@ -241,6 +241,34 @@ def summary(m, spec, logit_scale, dtype):
     }
 
 
+def selection_ablation(layer, spec, stream):
+    """The max threshold against the top-k and top-p rules (the V1 summary's
+    section 4.4 comparison), on one layer: kept density, attention time, and
+    the relative error of O against the exact dense output (every 64th token)."""
+    import torch
+    from block_sparse_long_fp_gb300 import fprefill
+    dense, _ = layer.dense_attn(want_lse=False)
+    rows = torch.arange(0, layer.total_q, 64, device=dense.device)
+    ref = dense[rows].float()
+    k_mean, v_mean, score = layer.discover()
+    saved = (layer.params.select_rule, layer.params.top_k, layer.params.top_p)
+    out = {}
+    rules = [("threshold_alpha_0.1", fprefill.FP_SELECT_THRESHOLD, 0, 0.0),
+             ("top_k_64", fprefill.FP_SELECT_TOPK, 64, 0.0),
+             ("top_p_0.9", fprefill.FP_SELECT_TOPP, 0, 0.9),
+             ("top_p_0.5", fprefill.FP_SELECT_TOPP, 0, 0.5)]
+    for name, rule, k, p in rules:
+        layer.params.select_rule, layer.params.top_k, layer.params.top_p = rule, k, p
+        rp, ci, nnz = layer.select(score)
+        o, _ = layer.sparse_attn(rp, ci, k_mean, v_mean, want_lse=False)
+        ms = cuda_time(lambda: layer.sparse_attn(rp, ci, k_mean, v_mean, out=o, want_lse=False), 3, stream)
+        stats = index_stats(spec, rp.cpu().numpy())
+        err = float(torch.linalg.vector_norm(o[rows].float() - ref) / torch.linalg.vector_norm(ref))
+        out[name] = {"density": round(stats["density"], 5), "attn_ms": round(ms, 4), "rel_err_vs_dense": round(err, 5)}
+    layer.params.select_rule, layer.params.top_k, layer.params.top_p = saved
+    return out
+
+
 def chunk_variant(dev, stream, steps, dense_steps):
     """A chunked-prefill step at long context: 512 queries at position 130560
     (32/4 heads, the 128K layer's shape).  It has 64 work units for 152 SMs, so
@@ -315,6 +343,7 @@ def run_ours(args, rank, world):
             layer.q.mul_(16.0)                  # exact: a power of two
             variants["bf16_logit_scale_16"] = summary(
                 measure_layer(layer, spec, min(args.steps, 5), 2, args.dense_steps, stream), spec, 16.0, "bf16")
+            variants["bf16_logit_scale_16"]["selection_ablation"] = selection_ablation(layer, spec, stream)
             layer.q.div_(16.0)
         del layer
         torch.cuda.empty_cache()

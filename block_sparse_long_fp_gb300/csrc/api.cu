@@ -28,6 +28,9 @@ fp_status build_desc(const fp_problem *p, const fp_params *prm, BatchDesc *bd) {
     if (p->cu_seqlens_q[0] != 0) return FP_ERR_INVALID;
     if (prm->sink_tokens < 0 || prm->local_tokens < 0 || !(prm->alpha >= 0.f)) return FP_ERR_INVALID;
     if (prm->kv_splits < 0 || prm->kv_splits > FP_MAX_KV_SPLITS) return FP_ERR_INVALID;
+    if (prm->select_rule == FP_SELECT_TOPK && prm->top_k < 1) return FP_ERR_INVALID;
+    if (prm->select_rule == FP_SELECT_TOPP && !(prm->top_p > 0.f && prm->top_p <= 1.f)) return FP_ERR_INVALID;
+    if (prm->select_rule < FP_SELECT_THRESHOLD || prm->select_rule > FP_SELECT_TOPP) return FP_ERR_INVALID;
     memset(bd, 0, sizeof(*bd));
     bd->batch = p->batch;
     bd->h_q = p->h_q;
@@ -162,6 +165,9 @@ fp_params fp_default_params(void) {
     p.softmax_scale = 0.f;
     p.mean_correction = 1;
     p.kv_splits = 0;
+    p.select_rule = FP_SELECT_THRESHOLD;
+    p.top_k = 0;
+    p.top_p = 0.f;
     return p;
 }
 
@@ -240,8 +246,9 @@ fp_status fp_select(const fp_problem *p, const fp_params *prm, const float *scor
     const int sink_blocks = (prm->sink_tokens + kBlock - 1) / kBlock;
     const int local_blocks = (prm->local_tokens + kBlock - 1) / kBlock;
     int *counts = reinterpret_cast<int *>(static_cast<char *>(ws) + kWsHeaderBytes);
-    if (launch_select(bd, prm->alpha, sink_blocks, local_blocks, score, counts, row_ptr, col_idx, col_capacity,
-                      nnz_dev, dense_mask_opt, status_ptr(ws), (cudaStream_t)stream) != cudaSuccess)
+    if (launch_select(bd, prm->alpha, sink_blocks, local_blocks, prm->select_rule, prm->top_k, prm->top_p, score,
+                      counts, row_ptr, col_idx, col_capacity, nnz_dev, dense_mask_opt, status_ptr(ws),
+                      (cudaStream_t)stream) != cudaSuccess)
         return FP_ERR_CUDA;
     return FP_OK;
 }

@@ -10,9 +10,9 @@ cudaError_t launch_pool(const BatchDesc &bd, bool fp8, const void *k_cache, cons
 cudaError_t launch_score(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
                          long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
                          float *score, cudaStream_t st);
-cudaError_t launch_select(const BatchDesc &bd, float alpha, int sink_blocks, int local_blocks, const float *score,
-                          int *counts, int *row_ptr, int *col_idx, long long col_capacity, int *nnz,
-                          unsigned char *dense_mask, int *status, cudaStream_t st);
+cudaError_t launch_select(const BatchDesc &bd, float alpha, int sink_blocks, int local_blocks, int rule, int top_k,
+                          float top_p, const float *score, int *counts, int *row_ptr, int *col_idx,
+                          long long col_capacity, int *nnz, unsigned char *dense_mask, int *status, cudaStream_t st);
 size_t score_smem_bytes(int max_nkb);
 // tensor-core score map (bf16 inputs): the three bf16 terms of the means live in
 // a workspace of score_tc_terms_bytes()

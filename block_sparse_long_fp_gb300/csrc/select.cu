@@ -2,11 +2,14 @@
 // safety net (FlashPrefill V1 summary, section 3.2; V2 paper reading, section
 // 4: 256 sink tokens, 512 local tokens, alpha = 0.1) and the compaction of the
 // kept key blocks into a CSR index (V1 section 3.3 "index-driven physical
-// jump"; V2 section 4 CSR output).
+// jump"; V2 section 4 CSR output).  The top-k and top-p rules the V1 summary
+// (section 4.4) compares the threshold with are kept as ablations.
 //
 // Three launches, no host synchronisation: (1) one warp per row decides and
 // counts, (2) one CTA scans the counts into row_ptr, (3) one warp per row
 // repeats the identical decision and writes its kept blocks at row_ptr[row].
+#include <limits.h>
+
 #include "common.cuh"
 #include "launch.cuh"
 
@@ -16,7 +19,28 @@ struct SelectArgs {
     float alpha;
     int sink_blocks;
     int local_blocks;
+    int rule;                 // fp_select_rule
+    int top_k;
+    float top_p;
 };
+
+// A row's decision: keep J when s > t, or s == t and J <= jt (jt: the last of
+// the equal scores that still fit, top-k only), or J is a sink / local block.
+struct RowRule {
+    float t;
+    int jt;
+};
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
 
 // Row maximum of a score row, reduced across the warp in a fixed order.
 __device__ __forceinline__ float warp_row_max(const float *s, int n, int lane) {
@@ -27,8 +51,68 @@ __device__ __forceinline__ float warp_row_max(const float *s, int n, int lane) {
     return mx;
 }
 
-__device__ __forceinline__ bool keep_block(float s, float thr, int J, int I, const SelectArgs &a) {
-    return s >= thr || J < a.sink_blocks || J >= I - a.local_blocks + 1;
+// Scores are >= 0, so their bit patterns order like their values: the top-k
+// and top-p thresholds are found by a binary search over the bit pattern (31
+// steps), each step one pass over the row by the warp.  Every kernel that
+// decides a row calls this with the same row, so all reach the same decision.
+__device__ RowRule row_rule(const float *s, int n, int lane, const SelectArgs &a) {
+    RowRule rr{0.f, INT_MAX};
+    if (a.rule == FP_SELECT_THRESHOLD) {
+        rr.t = a.alpha * warp_row_max(s, n, lane);      // keep s >= alpha * max
+        return rr;
+    }
+    unsigned lo = 0u, hi = 0x7f800000u;
+    if (a.rule == FP_SELECT_TOPK) {
+        const int k = a.top_k < n ? a.top_k : n;
+        while (lo < hi) {                                // the largest u with #(bits >= u) >= k
+            const unsigned mid = lo + (hi - lo + 1u) / 2u;
+            int c = 0;
+            for (int J = lane; J < n; J += 32) c += __float_as_uint(__ldg(s + J)) >= mid;
+            if (warp_sum(c) >= k) lo = mid;
+            else hi = mid - 1u;
+        }
+        rr.t = __uint_as_float(lo);
+        int gt = 0;
+        for (int J = lane; J < n; J += 32) gt += __float_as_uint(__ldg(s + J)) > lo;
+        const int need = k - warp_sum(gt);              // equal scores to keep, lowest J first (>= 1)
+        int seen = 0;
+        rr.jt = -1;
+        for (int J0 = 0; J0 < n; J0 += 32) {
+            const int J = J0 + lane;
+            const unsigned m = __ballot_sync(0xffffffffu, J < n && __float_as_uint(__ldg(s + J)) == lo);
+            const int c = __popc(m);
+            if (seen + c >= need) {
+                unsigned mm = m;
+                for (int q = 1; q < need - seen; ++q) mm &= mm - 1u;
+                rr.jt = J0 + __ffs(mm) - 1;
+                break;
+            }
+            seen += c;
+        }
+        return rr;
+    }
+    // top-p: the largest u whose scores >= u hold top_p of the row's total.  A
+    // subset's sum never rounds above its superset's (same order, adding
+    // non-negative terms), so the mass is monotone in u.
+    float tot = 0.f;
+    for (int J = lane; J < n; J += 32) tot += __ldg(s + J);
+    const float target = a.top_p * warp_sum(tot);
+    while (lo < hi) {
+        const unsigned mid = lo + (hi - lo + 1u) / 2u;
+        float m = 0.f;
+        for (int J = lane; J < n; J += 32) {
+            const float v = __ldg(s + J);
+            m += __float_as_uint(v) >= mid ? v : 0.f;
+        }
+        if (warp_sum(m) >= target) lo = mid;
+        else hi = mid - 1u;
+    }
+    rr.t = __uint_as_float(lo);
+    return rr;
+}
+
+__device__ __forceinline__ bool keep_block(float s, const RowRule &rr, int J, int I, const SelectArgs &a) {
+    return s > rr.t || (s == rr.t && J <= rr.jt) || J < a.sink_blocks || J >= I - a.local_blocks + 1;
 }
 
 __global__ void __launch_bounds__(256)
@@ -44,10 +128,10 @@ select_count_kernel(const __grid_constant__ BatchDesc bd, SelectArgs a, const fl
     const int I = rq.start / kBlock + i;
     const long long off = score_row_offset(rq, bd.h_kv, i, h);
     const float *s = score + off;
-    const float thr = a.alpha * warp_row_max(s, I + 1, lane);
+    const RowRule rr = row_rule(s, I + 1, lane, a);
     int cnt = 0;
     for (int J = lane; J <= I; J += 32) {
-        bool k = keep_block(__ldg(s + J), thr, J, I, a);
+        bool k = keep_block(__ldg(s + J), rr, J, I, a);
         cnt += k;
         if (dense_mask) dense_mask[off + J] = (unsigned char)k;
     }
@@ -110,7 +194,7 @@ select_compact_kernel(const __grid_constant__ BatchDesc bd, SelectArgs a, const 
     const int i = local / bd.h_kv, h = local % bd.h_kv;
     const int I = rq.start / kBlock + i;
     const float *s = score + score_row_offset(rq, bd.h_kv, i, h);
-    const float thr = a.alpha * warp_row_max(s, I + 1, lane);
+    const RowRule rr = row_rule(s, I + 1, lane, a);
     int pos = row_ptr[row];
     if ((long long)row_ptr[row + 1] > col_capacity) {
         if (lane == 0) set_status(status, FP_ERR_INVALID);
@@ -118,18 +202,18 @@ select_compact_kernel(const __grid_constant__ BatchDesc bd, SelectArgs a, const 
     }
     for (int J0 = 0; J0 <= I; J0 += 32) {
         int J = J0 + lane;
-        bool k = J <= I && keep_block(__ldg(s + J), thr, J, I, a);
+        bool k = J <= I && keep_block(__ldg(s + J), rr, J, I, a);
         unsigned m = __ballot_sync(0xffffffffu, k);
         if (k) col_idx[pos + __popc(m & ((1u << lane) - 1u))] = J;
         pos += __popc(m);
     }
 }
 
-cudaError_t launch_select(const BatchDesc &bd, float alpha, int sink_blocks, int local_blocks,
-                          const float *score, int *counts, int *row_ptr, int *col_idx,
+cudaError_t launch_select(const BatchDesc &bd, float alpha, int sink_blocks, int local_blocks, int rule,
+                          int top_k, float top_p, const float *score, int *counts, int *row_ptr, int *col_idx,
                           long long col_capacity, int *nnz, unsigned char *dense_mask, int *status,
                           cudaStream_t st) {
-    SelectArgs a{alpha, sink_blocks, local_blocks};
+    SelectArgs a{alpha, sink_blocks, local_blocks, rule, top_k, top_p};
     int grid = (bd.total_rows + 7) / 8;
     select_count_kernel<<<grid, 256, 0, st>>>(bd, a, score, counts, dense_mask);
     scan_kernel<<<1, 1024, 0, st>>>(counts, bd.total_rows, row_ptr, nnz);

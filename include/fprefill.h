@@ -99,7 +99,21 @@ typedef struct {
                              parts merged by their LSE (split-KV); 0 chooses (more
                              parts when the problem has too few work units to fill
                              the GPU), 1 never splits; at most FP_MAX_KV_SPLITS */
+    int select_rule;      /* fp_select rule (fp_select_rule); sink and local blocks are
+                             kept under every rule */
+    int top_k;            /* FP_SELECT_TOPK: blocks kept per row (>= 1) */
+    float top_p;          /* FP_SELECT_TOPP: share of the row's score mass kept, (0, 1] */
 } fp_params;
+
+/* Selection rules of fp_select.  THRESHOLD is the method's rule [V1 summary
+ * 3.2]; TOPK and TOPP are the alternatives it is compared with [V1 summary
+ * 4.4], kept here as ablations. */
+typedef enum {
+    FP_SELECT_THRESHOLD = 0,  /* Score >= alpha * max_J Score */
+    FP_SELECT_TOPK = 1,       /* the top_k highest scores; among equal scores the lower J */
+    FP_SELECT_TOPP = 2        /* the highest scores, down to the largest t such that the
+                                 scores >= t hold at least top_p of the row's total */
+} fp_select_rule;
 
 #define FP_MAX_KV_SPLITS 32
 
@@ -130,7 +144,7 @@ typedef struct {
 
 /* Defaults of the pages: B=128, sink 256, local 512, alpha 0.1, 1/sqrt(d),
  * mean correction on [V2 paper reading, section 4 configuration]; kv_splits 0
- * (chosen by the library). */
+ * (chosen by the library); the threshold rule (top_k 0, top_p 0: unused). */
 fp_params fp_default_params(void);
 
 /* Sizes derived from the host descriptors (element counts, not bytes). */
@@ -162,8 +176,12 @@ fp_status fp_discover(const fp_problem *p, const fp_params *prm, float *k_mean, 
  * [V1 3.2 threshold alpha * max_{J<=I} Score[I,J], sink and local safety net;
  *  V1 3.3 compaction of kept indices; V2 4 CSR index]
  *
- *   keep[I,J] = Score[I,J] >= alpha * max_J Score[I,J]
- *               or J * B < sink_tokens  or  J >= I - ceil(local_tokens / B) + 1
+ *   keep[I,J] = sel(I,J)  or  J * B < sink_tokens  or  J >= I - ceil(local_tokens / B) + 1
+ *   sel: FP_SELECT_THRESHOLD  Score[I,J] >= alpha * max_J Score[I,J];
+ *        FP_SELECT_TOPK  J is among the top_k highest scores of the row
+ *                        (equal scores: lower J first);
+ *        FP_SELECT_TOPP  Score[I,J] >= t, t the largest value such that the
+ *                        scores >= t sum to at least top_p * sum_J Score[I,J].
  *   row_ptr (device int32 [R + 1]), col_idx (device int32, col_capacity
  *   entries; the first nnz are written), nnz_dev (device int32 [1]).
  *   dense_mask_opt (device uint8, fp_score_size() bytes, may be NULL): the

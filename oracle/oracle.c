@@ -125,6 +125,73 @@ void oracle_select_row(const double *score, long I, double alpha, int B, int sin
 }
 
 /*
+ * Alternative selection rules [V1 4.4 compares the max threshold with top-k
+ * and top-p selection]; kept as ablations.  For the row scores s[0..I]:
+ *   rule 1, top-k: the min(k, I+1) highest scores, equal scores lowest J first;
+ *   rule 2, top-p: every J with s[J] >= t, t the highest score such that the
+ *                  scores >= t sum to at least p * sum_J s[J];
+ * rule 0 is the threshold rule above.  Sink and local blocks are kept under
+ * every rule.  flag[J] marks decisions that sit within rounding of the
+ * boundary: |s[J] - t| <= 1e-5 (the scores lie in (0, 1]), and for top-p a
+ * running mass (descending order, before or after J) within 1e-4 * total of
+ * the target.
+ */
+static const double *g_sort_scores;
+
+static int by_score_desc(const void *a, const void *b)
+{
+    long i = *(const long *)a, j = *(const long *)b;
+    double si = g_sort_scores[i], sj = g_sort_scores[j];
+    if (si > sj) return -1;
+    if (si < sj) return 1;
+    return (i > j) - (i < j);
+}
+
+void oracle_select_row_rule(const double *score, long I, int rule, double alpha, int top_k,
+                            double top_p, int B, int sink, int local, unsigned char *keep,
+                            unsigned char *flag)
+{
+    if (rule == 0) {
+        oracle_select_row(score, I, alpha, B, sink, local, keep, flag);
+        return;
+    }
+    long n = I + 1;
+    long *order = malloc((size_t)n * sizeof(long));
+    for (long J = 0; J < n; ++J) order[J] = J;
+    g_sort_scores = score;             /* the oracle runs rows one at a time here */
+    qsort(order, (size_t)n, sizeof(long), by_score_desc);
+    for (long J = 0; J < n; ++J) keep[J] = flag[J] = 0;
+    double t;
+    if (rule == 1) {
+        long k = top_k < n ? top_k : n;
+        t = score[order[k - 1]];
+        for (long q = 0; q < k; ++q) keep[order[q]] = 1;
+    } else {
+        double total = 0.0;
+        for (long J = 0; J < n; ++J) total += score[J];
+        double target = top_p * total, cum = 0.0;
+        long q = 0;
+        while (q < n - 1 && cum + score[order[q]] < target) cum += score[order[q++]];
+        t = score[order[q]];
+        for (long J = 0; J < n; ++J) keep[J] = score[J] >= t;
+        cum = 0.0;
+        for (q = 0; q < n; ++q) {
+            double before = cum;
+            cum += score[order[q]];
+            if (fabs(before - target) <= 1e-4 * total || fabs(cum - target) <= 1e-4 * total)
+                flag[order[q]] = 1;
+        }
+    }
+    long sink_blocks = ceil_div(sink, B);
+    long local_blocks = ceil_div(local, B);
+    for (long J = 0; J < n; ++J) {
+        if (fabs(score[J] - t) <= 1e-5) flag[J] = 1;
+        if (J < sink_blocks || J >= I - local_blocks + 1) keep[J] = 1;
+    }
+    free(order);
+}
+
+/*
  * Sparse attention with block-mean correction for selected query rows
  * [V2 4.1; V2p mean correction], written as the plain ratio of sums:
  *

@@ -10,7 +10,8 @@ Parity status of each function (what pins it; see tests/test_oracle_pins.py):
   score_rows   pinned: hand-derived closed form (tests/golden/score_tiny.json),
                per-query shift invariance, head/query permutation invariance,
                row maximum exactly 1.
-  select_row   pinned: brute-force rule check, sink/local/causal invariants.
+  select_row   pinned: brute-force rule check, sink/local/causal invariants;
+               top-k / top-p: count, dominance, tie order, minimal mass, limits.
   attn_rows    pinned: alpha=0 equals direct dense causal softmax; exact mean
                correction for constant-key blocks; token-level brute force
                with appended "mean tokens" at L <= 512; V-linearity.
@@ -55,6 +56,7 @@ def _load():
         _lib.oracle_pool.argtypes = [P, L, I, I, I, P]
         _lib.oracle_score_rows.argtypes = [P, L, L, I, I, I, I, D, P, L, P, L, P, P]
         _lib.oracle_select_row.argtypes = [P, L, D, I, I, I, P, P]
+        _lib.oracle_select_row_rule.argtypes = [P, L, I, D, I, D, I, I, I, P, P]
         _lib.oracle_attn_rows.argtypes = [P, L, L, I, I, I, I, D, P, P, L, P, P, L, P, I,
                                           P, P, L, P, P]
     return _lib
@@ -148,11 +150,17 @@ def score_rows(q, start, hkv, B, scale, kbar, rows):
     return [out[o:o + n] for o, n in zip(off, lens)]
 
 
-def select_row(score_row: np.ndarray, I: int, alpha: float, B: int, sink: int, local: int):
+def select_row(score_row: np.ndarray, I: int, alpha: float, B: int, sink: int, local: int, rule: int = 0,
+               top_k: int = 0, top_p: float = 0.0):
+    """keep / flag masks of one score row: rule 0 the max threshold, 1 top-k,
+    2 top-p (the last two as ablations)."""
     s = np.ascontiguousarray(score_row, dtype=np.float64)
     keep = np.zeros(I + 1, dtype=np.uint8)
     flag = np.zeros(I + 1, dtype=np.uint8)
-    _load().oracle_select_row(_p(s), I, alpha, B, sink, local, _p(keep), _p(flag))
+    if rule == 0:
+        _load().oracle_select_row(_p(s), I, alpha, B, sink, local, _p(keep), _p(flag))
+    else:
+        _load().oracle_select_row_rule(_p(s), I, rule, alpha, top_k, top_p, B, sink, local, _p(keep), _p(flag))
     return keep.astype(bool), flag.astype(bool)
 
 
@@ -213,7 +221,7 @@ def csr_from_keep(keep_rows):
 
 
 def discover_and_select(case, B=128, sink=256, local=512, alpha=0.1, scale=None,
-                        requests_subset=None, row_subset=None):
+                        requests_subset=None, row_subset=None, rule=0, top_k=0, top_p=0.0):
     """Steps 1-3 for every request (or a subset): block means, score rows,
     keep / flag masks.  Returns a dict with per-request results."""
     spec = case.spec
@@ -235,7 +243,7 @@ def discover_and_select(case, B=128, sink=256, local=512, alpha=0.1, scale=None,
         for row, s in zip(rows, srows):
             i, h = divmod(int(row), hkv)
             I = start // B + i
-            kp, fl = select_row(s, I, alpha, B, sink, local)
+            kp, fl = select_row(s, I, alpha, B, sink, local, rule, top_k, top_p)
             keep[i, h, :I + 1] = kp
             flag[i, h, :I + 1] = fl
             have[i, h] = True

@@ -22,12 +22,15 @@ def built():
 
 
 def full_parity(spec, alpha=0.1, mean_corr=True, rows_per_request=None, max_abs=None, mean_abs=None,
-                lse_abs=2e-2):
+                lse_abs=2e-2, select=None):
+    """select: {select_rule, top_k, top_p} for the top-k / top-p ablations."""
     import oracle
     from parity_util import BF16_MAX_ABS, BF16_MEAN_ABS
     case = synth.make_case(spec)
-    ref = oracle.discover_and_select(case, alpha=alpha)
-    g = gpu_stage_outputs(case, alpha=alpha, mean_corr=mean_corr)
+    sel = select or {}
+    ref = oracle.discover_and_select(case, alpha=alpha, rule=sel.get("select_rule", 0), top_k=sel.get("top_k", 0),
+                                     top_p=sel.get("top_p", 0.0))
+    g = gpu_stage_outputs(case, alpha=alpha, mean_corr=mean_corr, select=select)
     assert g["status"] == 0
     check_pool(case, g, ref)
     flips = check_scores_and_index(case, g, ref)
@@ -192,6 +195,28 @@ def test_split_kv_chunk_at_the_end_of_a_long_context(dtype, logit_scale):
     fp8 = dtype == "e4m3"
     full_parity(spec, rows_per_request=700, max_abs=FP8_MAX_ABS if fp8 else None, mean_abs=6e-3 if fp8 else None,
                 lse_abs=FP8_LSE_ABS if fp8 else 2e-2)
+
+
+@pytest.mark.parametrize("select,mean_corr", [(dict(select_rule=1, top_k=1), False), (dict(select_rule=1, top_k=8), True),
+                                              (dict(select_rule=2, top_p=0.5), True),
+                                              (dict(select_rule=2, top_p=0.9), True)])
+def test_topk_topp_selection_ablations(select, mean_corr):
+    """The top-k and top-p rules (ablations of the max threshold): the GPU's
+    index equals the oracle's outside the flagged boundary band, and the
+    attention on it matches.  With one kept block per row a row is nearly all
+    mean tokens, whose keys enter the bf16 MMA rounded to bf16 (a logit error
+    up to 2^-9 * scale * sum_c |q_c kmean_c|, ~0.09 here): that case checks
+    the attention without the correction, exact over the kept blocks."""
+    spec = synth.Spec("sharp-8k", [(8192, 0)], 4, 1, page_size=64, layout="shuffled", n_needles=2,
+                      logit_scale=8.0, config_id=1)
+    full_parity(spec, rows_per_request=1500, select=select, mean_corr=mean_corr)
+
+
+@pytest.mark.parametrize("select", [dict(select_rule=1, top_k=3), dict(select_rule=2, top_p=0.7)])
+def test_topk_topp_on_a_ragged_varlen_batch(select):
+    spec = synth.Spec("varlen-small", [(300, 0), (1000, 0), (256, 512), (1, 128), (640, 0)], 8, 2,
+                      page_size=32, layout="interleaved", n_needles=2, logit_scale=6.0, config_id=92)
+    full_parity(spec, select=select)
 
 
 def test_page_table_entry_out_of_range_sets_status():

@@ -184,6 +184,62 @@ def test_select_threshold_is_inclusive_and_flags_band(oracle_mod):
     assert list(flag) == [False, False, True, True, False, False, False, False, False, False]
 
 
+@pytest.mark.parametrize("k", [1, 3, 7, 40, 55])
+def test_topk_keeps_the_k_highest_lowest_index_first(oracle_mod, k):
+    """Top-k (V1 summary 4.4 ablation), no forced blocks: exactly min(k, n)
+    blocks; every kept score >= every dropped one; among equal scores at the
+    boundary the kept ones have the lower indices."""
+    rng = np.random.default_rng(11)
+    for I in [0, 5, 40]:
+        s = np.round(rng.random(I + 1), 1) + 0.05      # many ties on a 0.1 grid
+        keep, flag = oracle_mod.select_row(s, I, 0.1, 128, 0, 0, rule=1, top_k=k)
+        n = I + 1
+        assert keep.sum() == min(k, n)
+        if keep.all():
+            continue
+        assert s[keep].min() >= s[~keep].max()
+        t = s[keep].min()
+        tied = np.nonzero(s == t)[0]
+        kept_tied, dropped_tied = tied[keep[tied]], tied[~keep[tied]]
+        if len(dropped_tied):
+            assert kept_tied.max() < dropped_tied.min()
+        assert flag[tied].all()                          # the boundary value is flagged
+
+
+@pytest.mark.parametrize("p", [1e-6, 0.3, 0.6, 0.9, 1.0])
+def test_topp_keeps_the_smallest_top_set_holding_p_of_the_mass(oracle_mod, p):
+    """Top-p (V1 summary 4.4 ablation), no forced blocks: the kept set holds
+    at least p of the row's mass, dropping its lowest value (with its ties)
+    falls short, and every kept score >= every dropped one."""
+    rng = np.random.default_rng(12)
+    for I in [0, 6, 60]:
+        s = rng.random(I + 1) ** 3 + 1e-3
+        keep, flag = oracle_mod.select_row(s, I, 0.1, 128, 0, 0, rule=2, top_p=p)
+        total = s.sum()
+        assert s[keep].sum() >= p * total * (1 - 1e-12)
+        t = s[keep].min()
+        assert s[s > t].sum() < p * total
+        if not keep.all():
+            assert t >= s[~keep].max()
+        if p == 1.0:
+            assert keep.all()
+        if p == 1e-6:
+            assert keep.sum() == np.sum(s == s.max())
+
+
+def test_topk_topp_keep_sink_and_local_blocks(oracle_mod):
+    rng = np.random.default_rng(13)
+    I = 30
+    s = rng.random(I + 1)
+    for rule, kw in ((1, dict(top_k=2)), (2, dict(top_p=0.2))):
+        keep, _ = oracle_mod.select_row(s, I, 0.1, 128, 256, 512, rule=rule, **kw)
+        alone, _ = oracle_mod.select_row(s, I, 0.1, 128, 0, 0, rule=rule, **kw)
+        forced = np.zeros(I + 1, bool)
+        forced[:2] = True
+        forced[I - 3:] = True
+        assert np.array_equal(keep, alone | forced)
+
+
 # ----------------------------------------------------------------------------
 # attention
 # ----------------------------------------------------------------------------
