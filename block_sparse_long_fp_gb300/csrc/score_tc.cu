@@ -27,6 +27,8 @@
 // from shared memory); there are two query buffers, and the next pair's
 // queries (prefetched into L2 when the pair starts) go in at the start of
 // this pair's second pass, so the tensor cores never wait for them.
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.cuh"
 #include "sm100.cuh"
@@ -119,35 +121,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 // Column sums of a 32x32 block held one row per lane (v[c] = column c of
 // this lane's row): after the butterfly, lane L holds the sum of column L.
+// Each stage halves the columns a lane holds: it keeps one half, sends the
+// other to its partner and adds what it receives, in pairs (add.rn.f32x2),
+// each sum rounded exactly as a scalar add would.
 __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
+    auto stage = [&](auto half_c, int mask) {
+        constexpr int h = decltype(half_c)::value;
+        const bool up = lane & mask;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const bool up = lane & 16;
-        const float send = up ? v[k] : v[k + 16];
-        const float keep = up ? v[k + 16] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const bool up = lane & 8;
-        const float send = up ? v[k] : v[k + 8];
-        const float keep = up ? v[k + 8] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const bool up = lane & 4;
-        const float send = up ? v[k] : v[k + 4];
-        const float keep = up ? v[k + 4] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const bool up = lane & 2;
-        const float send = up ? v[k] : v[k + 2];
-        const float keep = up ? v[k + 2] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
+        for (int k = 0; k < h; k += 2) {
+            const float r0 = __shfl_xor_sync(0xffffffffu, up ? v[k] : v[k + h], mask);
+            const float r1 = __shfl_xor_sync(0xffffffffu, up ? v[k + 1] : v[k + 1 + h], mask);
+            float a0, a1;
+            f2_unpack(f2_add(f2_pack(up ? v[k + h] : v[k], up ? v[k + 1 + h] : v[k + 1]), f2_pack(r0, r1)), a0, a1);
+            v[k] = a0;
+            v[k + 1] = a1;
+        }
+    };
+    stage(std::integral_constant<int, 16>{}, 16);
+    stage(std::integral_constant<int, 8>{}, 8);
+    stage(std::integral_constant<int, 4>{}, 4);
+    stage(std::integral_constant<int, 2>{}, 2);
     const bool up = lane & 1;
     const float send = up ? v[0] : v[1];
     const float keep = up ? v[1] : v[0];
@@ -350,7 +344,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
             float mc2 = 0.f;
             for (int pass = 0; pass < 2 && ok; ++pass) {
                 if (pass == 1) {
-                    mc2 = (m == -INFINITY || !row_valid) ? 0.f : m * c2;
+                    mc2 = !row_valid ? INFINITY : (m == -INFINITY ? 0.f : m * c2);
                     // the next pair's queries go into the other buffer while this
                     // pair's second pass keeps the tensor cores busy
                     if (next && !put_queries(pr + 1)) { ok = false; break; }
@@ -383,14 +377,27 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                         }
                         m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                     } else {
+                        // exponents as paired FMAs: (s0, s1) * c2 - mc2 (an invalid row
+                        // has mc2 = +inf, so its terms are exactly 0); columns past
+                        // the row are masked only in its last, partial chunk
+                        const uint64_t cc = f2_pack(c2, c2), nm = f2_pack(-mc2, -mc2);
 #pragma unroll
                         for (int sl = 0; sl < kChunk / 32; ++sl) {
                             const int J0 = c * kChunk + sl * 32;
                             float v0[32];
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                v0[e] = (row_valid && J0 + e < ncol) ? fast_exp2(fmaf(__uint_as_float(sv[sl][e]), c2, -mc2))
-                                                                      : 0.f;
+                            for (int e = 0; e < 32; e += 2) {
+                                float z0, z1;
+                                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[sl][e]), __uint_as_float(sv[sl][e + 1])), cc, nm),
+                                          z0, z1);
+                                v0[e] = fast_exp2(z0);
+                                v0[e + 1] = fast_exp2(z1);
+                            }
+                            if (J0 + 32 > ncol) {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e)
+                                    if (J0 + e >= ncol) v0[e] = 0.f;
+                            }
                             // lane L now gets the sum of column J0 + L over this warp's 32 rows
                             const float s0 = transpose_reduce32(v0, lane);
                             if (J0 + lane < ncol) my_acc[J0 + lane] += s0;
