@@ -229,6 +229,13 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     const Unit U = decode_unit(bd, a, unit);
                     n_kept = U.n_kept;
                     split = U.split;
+                    // the unit's queries into L2 now, so that their load when the
+                    // unit starts (exposed, at a unit switch) hits L2, not DRAM
+                    if (lane == 0) {
+                        const int q_row0 = bd.req[U.r].q_off + U.il * kBlock;
+                        for (int t = 0; t < 2; ++t)
+                            for (int hf = 0; hf < kNH; ++hf) tma_prefetch_l2_3d(&tmQ, hf * 64, U.hq0 + t, q_row0);
+                    }
                     const int I = U.I;
                     if (sparse && a.mean_corr && I > 0) {
                         const int nw = (I + 31) / 32;
