@@ -77,6 +77,7 @@ struct UnitMeta {
     int jb;                           // the part's first term in the row's list
     int n_kept;                       // kept blocks of the row (terms before the mean tiles)
     int pad[2];
+    int z0[32];                       // first lookup round: pool row of box (term jb + k / nsub, k % nsub)
     uint32_t bitmap[kBitmapWords];    // kept blocks J < I
     int corr[kMaxCorrTiles];          // mean tiles holding a skipped block
 };
@@ -264,11 +265,33 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         }
                     }
                 }
+                // this part's share of the row's terms
+                const int n_terms = n_kept + n_corr;
+                const int jb = (int)((long long)split * n_terms / a.n_split);
+                const int je = (int)((long long)(split + 1) * n_terms / a.n_split);
+                if (!end) {
+                    // the first round of page lookups, ahead of the producer (the
+                    // same rule as its own rounds: one box per lane)
+                    const Unit U = decode_unit(bd, a, unit);
+                    const ReqDesc &rq = bd.req[U.r];
+                    const int rpb = a.page_size < kBlock ? a.page_size : kBlock;
+                    const int nsub = kBlock / rpb;
+                    const int jj = jb + lane / nsub;
+                    int z = a.num_pages * a.page_size;                 // zero-filled rows
+                    if (jj < n_kept) {
+                        const int J = sparse ? __ldg(a.col_idx + U.rp0 + jj) : jj;
+                        const int tok = J * kBlock + (lane % nsub) * rpb;
+                        const int lp = tok / a.page_size;
+                        const int npages_req = (rq.lk + a.page_size - 1) / a.page_size;
+                        if (tok < rq.lk && lp < npages_req) {
+                            const int pg = __ldg(a.block_table + (long long)U.r * a.max_pages + lp);
+                            if (pg >= 0 && pg < a.num_pages) z = pg * a.page_size + tok % a.page_size;
+                            else set_status(a.status, FP_ERR_DEVICE_BOUNDS);
+                        }
+                    }
+                    M.z0[lane] = z;
+                }
                 if (lane == 0) {
-                    // this part's share of the row's terms
-                    const int n_terms = n_kept + n_corr;
-                    const int jb = (int)((long long)split * n_terms / a.n_split);
-                    const int je = (int)((long long)(split + 1) * n_terms / a.n_split);
                     M.pos = end ? -1 : pos;
                     M.unit = unit;
                     M.n_items = je - jb;
@@ -350,15 +373,16 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         }
                     }
                     if (!__shfl_sync(0xffffffffu, good, 0)) break;
-                    // terms jb .. jb + n_items - 1 of the row (this unit's part)
+                    // terms jb .. jb + n_items - 1 of the row (this unit's part); the
+                    // metadata warp looked up the first round, this warp the rest
                     const int jb = M.jb;
                     int pg_n, off_n;
-                    look(jb, pg_n, off_n);
-                    int z_cur = oob;
+                    look(jb + per, pg_n, off_n);
+                    int z_cur = M.z0[lane];
                     for (int jl = 0; jl < n_items && good; ++jl, ++it) {
                         const int j = jb + jl;
                         const int lj = jl % per;
-                        if (lj == 0) {                      // next round: take it, look up the one after
+                        if (lj == 0 && jl > 0) {            // next round: take it, look up the one after
                             z_cur = row_of(pg_n, off_n);
                             look(j + per, pg_n, off_n);
                         }
