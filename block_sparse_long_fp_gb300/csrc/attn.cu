@@ -633,13 +633,29 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         if (!((w[e >> 5] >> (e & 31)) & 1u)) x[e] = -INFINITY;
                     bias = 7.f;
                 }
-                // row max: eight independent chains of three-input max, then a tree
-                float mx8[8];
+                // row max in independent chains of three-input max, then a tree:
+                // sixteen chains (at most four deep) for bf16; eight for e4m3,
+                // whose exponent loop leaves fewer registers
+                float mxr;
+                if constexpr (!kFp8) {
+                    float mx16[16];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) mx8[q] = x[q];
+                    for (int q = 0; q < 16; ++q) mx16[q] = max3f(x[3 * q], x[3 * q + 1], x[3 * q + 2]);
 #pragma unroll
-                for (int e = 8; e < 128; e += 2) mx8[(e >> 1) & 7] = max3f(mx8[(e >> 1) & 7], x[e], x[e + 1]);
-                const float mxr = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+                    for (int e = 48; e < 128; e += 2)
+                        mx16[((e - 48) >> 1) & 15] = max3f(mx16[((e - 48) >> 1) & 15], x[e], x[e + 1]);
+                    mxr = max3f(max3f(max3f(mx16[0], mx16[1], mx16[2]), max3f(mx16[3], mx16[4], mx16[5]),
+                                      max3f(mx16[6], mx16[7], mx16[8])),
+                                max3f(mx16[9], mx16[10], mx16[11]),
+                                max3f(max3f(mx16[12], mx16[13], mx16[14]), mx16[15], mx16[15]));
+                } else {
+                    float mx8[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) mx8[q] = x[q];
+#pragma unroll
+                    for (int e = 8; e < 128; e += 2) mx8[(e >> 1) & 7] = max3f(mx8[(e >> 1) & 7], x[e], x[e + 1]);
+                    mxr = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+                }
                 const float mx = mxr * csc + bias;                   // log2 units; -inf stays -inf
                 // grow the running max only when it rises by more than 2^8 (rarely);
                 // O is rescaled after P is written (x is dead by then), and the
