@@ -213,6 +213,9 @@ def measure_layer(layer, spec, steps, warmup, dense_steps, stream, fp8=False):
     ms_sel = cuda_time(lambda: layer.select(score, rp, ci, nz), reps, stream)
     ms_attn = cuda_time(lambda: layer.sparse_attn(rp, ci, k_mean, v_mean, out=out_buf, want_lse=False), reps,
                         stream)
+    # the fused fp_discover_select (no score map) in place of the first two stages
+    km2, vm2, rp2, ci2, nz2 = layer.discover_select()
+    ms_dsel = cuda_time(lambda: layer.discover_select(km2, vm2, None, rp2, ci2, nz2), reps, stream)
     ms_dense = None
     if dense_steps > 0:
         layer.dense_attn(out=out_buf, want_lse=False)
@@ -222,7 +225,7 @@ def measure_layer(layer, spec, steps, warmup, dense_steps, stream, fp8=False):
     attn_flop = stats["kept_flop"] + stats["corr_flop"]
     achieved = attn_flop / (ms_attn * 1e-3) / 1e12
     return dict(ms=ms, flop=flop, status=status, stats=stats, ms_disc=ms_disc, ms_sel=ms_sel, ms_attn=ms_attn,
-                ms_dense=ms_dense, achieved=achieved, peak=peak, peak_kind=peak_kind)
+                ms_dense=ms_dense, ms_dsel=ms_dsel, achieved=achieved, peak=peak, peak_kind=peak_kind)
 
 
 def summary(m, spec, logit_scale, dtype):
@@ -231,7 +234,7 @@ def summary(m, spec, logit_scale, dtype):
         "ms_per_layer": round(m["ms"], 4),
         "dense_equiv_tflops": round(m["flop"] / (m["ms"] * 1e-3) / 1e12, 2),
         "stages_ms": {"discover": round(m["ms_disc"], 4), "select": round(m["ms_sel"], 4),
-                      "sparse_attn": round(m["ms_attn"], 4)},
+                      "sparse_attn": round(m["ms_attn"], 4), "discover_select_fused": round(m["ms_dsel"], 4)},
         "density": round(m["stats"]["density"], 5),
         "attn_tflops": round(m["achieved"], 2), "attn_peak_tflops": m["peak"],
         "attn_frac": round(m["achieved"] / m["peak"], 4),
@@ -379,7 +382,7 @@ def run_ours(args, rank, world):
                    "l2": f"inputs larger than L2 (Q alone is {q_bytes / 2**20:.0f} MiB)"},
         "ms_per_layer": round(ms, 4),
         "stages_ms": {"discover": round(ms_disc, 4), "select": round(ms_sel, 4),
-                      "sparse_attn": round(ms_attn, 4)},
+                      "sparse_attn": round(ms_attn, 4), "discover_select_fused": round(m["ms_dsel"], 4)},
         "density": round(stats["density"], 5), "nnz_blocks": stats["nnz"], "csr_bytes": stats["csr_bytes"],
         "dense_attn_ms": None if ms_dense is None else round(ms_dense, 4),
         "speedup_vs_own_dense": None if ms_dense is None else round(ms_dense / ms, 3),

@@ -253,6 +253,69 @@ fp_status fp_select(const fp_problem *p, const fp_params *prm, const float *scor
     return FP_OK;
 }
 
+size_t fp_discover_select_workspace_size(const fp_problem *p, const fp_params *prm) {
+    BatchDesc bd;
+    if (build_desc(p, prm, &bd) != FP_OK) return 0;
+    size_t n = align_up(fp_discover_workspace_size(p, prm), 256);
+    n += align_up((size_t)(bd.total_rows > 0 ? bd.total_rows : 1) * 8 * sizeof(int), 256);  // kept counts
+    n += align_up((size_t)(bd.score_size > 0 ? bd.score_size : 1) * sizeof(int), 256);    // kept lists / scores
+    return n;
+}
+
+fp_status fp_discover_select(const fp_problem *p, const fp_params *prm, float *k_mean, float *v_mean,
+                             float *score_opt, int *row_ptr, int *col_idx, long long col_capacity, int *nnz_dev,
+                             void *ws, size_t ws_bytes, void *stream) {
+    BatchDesc bd;
+    fp_status s = build_desc(p, prm, &bd);
+    if (s != FP_OK) return s;
+    if ((s = check_kv(p, bd)) != FP_OK || (s = check_q(p)) != FP_OK) return s;
+    if (!k_mean || !v_mean || !aligned16(k_mean) || !aligned16(v_mean)) return FP_ERR_INVALID;
+    if (!row_ptr || !col_idx || !nnz_dev || col_capacity < bd.score_size) return FP_ERR_INVALID;
+    if (!ws || ws_bytes < fp_discover_select_workspace_size(p, prm)) return FP_ERR_WORKSPACE;
+    const bool tc = use_score_tc(p, bd);
+    if (!tc && score_smem_bytes(bd.max_nkb) > 227 * 1024) return FP_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool fp8 = p->dtype == FP_E4M3;
+    char *w = static_cast<char *>(ws);
+    size_t off = align_up(fp_discover_workspace_size(p, prm), 256);
+    int *counts = reinterpret_cast<int *>(w + off);     // [rows, 8] (fused) or [rows]
+    off += align_up((size_t)(bd.total_rows > 0 ? bd.total_rows : 1) * 8 * sizeof(int), 256);
+    int *keep_pad = reinterpret_cast<int *>(w + off);
+    const int sink_blocks = (prm->sink_tokens + kBlock - 1) / kBlock;
+    const int local_blocks = (prm->local_tokens + kBlock - 1) / kBlock;
+    if (bd.total_kb > 0 &&
+        launch_pool(bd, fp8, p->k_cache, p->v_cache, p->page_size, p->num_pages, p->block_table,
+                    p->max_pages_per_seq, p->k_scale, p->v_scale, k_mean, v_mean, status_ptr(ws), st) != cudaSuccess)
+        return FP_ERR_CUDA;
+    if (bd.total_rows == 0) {
+        return cudaMemsetAsync(row_ptr, 0, sizeof(int), st) == cudaSuccess &&
+                       cudaMemsetAsync(nnz_dev, 0, sizeof(int), st) == cudaSuccess
+                   ? FP_OK
+                   : FP_ERR_CUDA;
+    }
+    __nv_bfloat16 *terms = reinterpret_cast<__nv_bfloat16 *>(w + kWsHeaderBytes);
+    const float scale = softmax_scale_of(prm, p->d);
+    cudaError_t e;
+    if (tc && prm->select_rule == FP_SELECT_THRESHOLD) {
+        // one pass: the score kernel decides each row and lists its kept blocks
+        ScoreSelect sel{keep_pad, counts, prm->alpha, sink_blocks, local_blocks};
+        e = launch_score_tc(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean, scale, score_opt,
+                            terms, status_ptr(ws), g_wait_ns, st, &sel);
+        if (e == cudaSuccess)
+            e = launch_select_gather(bd, keep_pad, counts, row_ptr, col_idx, col_capacity, nnz_dev, status_ptr(ws), st);
+    } else {
+        // the separate stages, with the score map in the workspace when none is given
+        float *sc = score_opt ? score_opt : reinterpret_cast<float *>(keep_pad);
+        e = tc ? launch_score_tc(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean, scale, sc,
+                                 terms, status_ptr(ws), g_wait_ns, st)
+               : launch_score(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean, scale, sc, st);
+        if (e == cudaSuccess)
+            e = launch_select(bd, prm->alpha, sink_blocks, local_blocks, prm->select_rule, prm->top_k, prm->top_p, sc,
+                              counts, row_ptr, col_idx, col_capacity, nnz_dev, nullptr, status_ptr(ws), st);
+    }
+    return e == cudaSuccess ? FP_OK : FP_ERR_CUDA;
+}
+
 int fp_attn_kv_splits(const fp_problem *p, const fp_params *prm) {
     BatchDesc bd;
     if (build_desc(p, prm, &bd) != FP_OK) return -1;

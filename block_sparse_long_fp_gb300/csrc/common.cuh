@@ -51,6 +51,10 @@ __device__ __forceinline__ void set_status(int *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+// Fused selection: a score row of ncol entries is cut into 8 segments of
+// this many (a multiple of 32), one per row warp of the score kernel.
+__host__ __device__ __forceinline__ int score_segment(int ncol) { return ((ncol + 7) / 8 + 31) / 32 * 32; }
+
 // Request owning global row `row` (rows are request-major).
 __device__ __forceinline__ int req_of_row(const BatchDesc &bd, int row) {
     int lo = 0, hi = bd.batch - 1;

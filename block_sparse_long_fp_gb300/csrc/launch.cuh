@@ -21,10 +21,19 @@ size_t score_tc_smem_bytes(int max_nkb);   // the tensor-core path needs this <=
 inline size_t score_tc_terms_bytes(const BatchDesc &bd) {
     return (size_t)3 * score_tc_rows_pad(bd) * bd.h_kv * kHeadDim * 2;
 }
+// fused selection at the end of the tensor-core score kernel (threshold rule)
+struct ScoreSelect {
+    int *keep_pad;            // [score_size] ints: each row's kept blocks at its score-map offset
+    int *counts;              // [total_rows, 8]: kept blocks per row warp's segment
+    float alpha;
+    int sink_blocks, local_blocks;
+};
 cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
                             long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
                             float *score, __nv_bfloat16 *terms, int *status, unsigned long long wait_ns,
-                            cudaStream_t st);
+                            cudaStream_t st, const ScoreSelect *sel = nullptr);
+cudaError_t launch_select_gather(const BatchDesc &bd, const int *keep_pad, const int *counts, int *row_ptr,
+                                 int *col_idx, long long col_capacity, int *nnz, int *status, cudaStream_t st);
 
 struct AttnLaunch {
     const BatchDesc *bd;

@@ -55,7 +55,7 @@ struct ScoreCfg {
     static constexpr int kTmemBufs = 2 * kBufs;
     static constexpr int kSmStage = 0;
     static constexpr int kSmCtl = kSmStage + kStages * kStageBytes;
-    static constexpr int kSmAcc = kSmCtl + 256;                // per-warp column sums [8][max_nkb]
+    static constexpr int kSmAcc = kSmCtl + 512;                // per-warp column sums [8][max_nkb]
     // TMEM: the S buffers (kBufs per head slot), then the query tiles as MMA
     // A operands (128 rows x 128 bf16 = 64 columns each), two buffers of two
     // head slots, so the next pair's queries go in while this pair runs
@@ -65,7 +65,7 @@ struct ScoreCfg {
     static constexpr int B_QF = 0, B_QE = 4, B_SF = 8, B_SE = 8 + kStages, B_TF = 8 + 2 * kStages;
     static constexpr int B_TE = B_TF + 4, B_N = B_TE + 4;
     static_assert(kTmemQ + 256 <= 512, "TMEM budget");
-    static_assert(B_N * 8 + 64 <= 256, "control block");
+    static_assert(B_N * 8 + 64 <= 512, "control block");
     static size_t smem_bytes(int max_nkb) { return (size_t)kSmAcc + 8 * sizeof(float) * max_nkb + 1024; }
 };
 
@@ -78,6 +78,13 @@ struct ScoreTcArgs {
     const float *q_scale;     // e4m3 only: per query head
     int rows_pad;             // rows of each mean term in the split array
     int acc_stride;           // floats per warp accumulator (>= the row length)
+    // fused selection (null: scores only): each row's kept blocks, ascending,
+    // into keep_pad at the row's score-map offset, and their count
+    int *keep_pad;
+    int *counts;
+    float alpha;
+    int sink_blocks;
+    int local_blocks;
     int *status;
     unsigned long long wait_ns;
 };
@@ -184,7 +191,8 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
     const int ncol = I + 1;
     const int nch = (ncol + kChunk - 1) / kChunk;
     const int g = bd.g;
-    float *out = a.score + score_row_offset(rq, bd.h_kv, il, h);
+    const long long row_off = score_row_offset(rq, bd.h_kv, il, h);
+    float *out = a.score ? a.score + row_off : nullptr;
 
     const int npairs = (g + 1) / 2;
     const int steps_per_pair = 2 * nch;
@@ -425,11 +433,34 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
 #pragma unroll
             for (int k = 0; k < 8; ++k) mx = fmaxf(mx, red[k]);
             const float inv = 1.f / mx;
-            if (ok2)
-                for (int J = t; J < ncol; J += 256) {
-                    const float v = colsum(J);
-                    out[J] = v == mx ? 1.f : v * inv;
+            auto score_of = [&](int J) {
+                const float v = colsum(J);
+                return v == mx ? 1.f : v * inv;
+            };
+            if (ok2 && !a.keep_pad) {
+                for (int J = t; J < ncol; J += 256) out[J] = score_of(J);
+            } else if (ok2) {
+                // fused selection [V1 summary 3.2-3.3]: the row's maximum is exactly 1,
+                // so a block is kept when its score >= alpha, or it is a sink or local
+                // block.  Row warp w takes segment w of the row (score_segment()),
+                // writes its kept blocks, ascending, from the segment's start, and
+                // records their count: no further sync, the gather joins the segments.
+                const int wr = warp - 4;
+                const int seg = score_segment(ncol);
+                const int j0 = wr * seg, j1 = min(ncol, j0 + seg);
+                int *dst = a.keep_pad + row_off + j0;
+                int pos = 0;
+                for (int J0 = j0; J0 < j1; J0 += 32) {
+                    const int J = J0 + lane;
+                    const float sc = J < j1 ? score_of(J) : 0.f;
+                    const bool k = J < j1 && (sc >= a.alpha || J < a.sink_blocks || J >= I - a.local_blocks + 1);
+                    if (J < j1 && out) out[J] = sc;
+                    const unsigned m = __ballot_sync(0xffffffffu, k);
+                    if (k) dst[pos + __popc(m & ((1u << lane) - 1u))] = J;
+                    pos += __popc(m);
                 }
+                if (lane == 0) a.counts[row * 8 + wr] = pos;
+            }
         }
     }
 
@@ -501,7 +532,7 @@ size_t score_tc_smem_bytes(int max_nkb) {
 cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
                             long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
                             float *score, __nv_bfloat16 *terms, int *status, unsigned long long wait_ns,
-                            cudaStream_t st) {
+                            cudaStream_t st, const ScoreSelect *sel) {
     const int rows_pad = score_tc_rows_pad(bd);
     const long long n = (long long)bd.total_kb * bd.h_kv * kHeadDim;
     const long long n_pad = (long long)rows_pad * bd.h_kv * kHeadDim;
@@ -523,6 +554,11 @@ cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long l
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
     a.rows_pad = rows_pad;
     a.acc_stride = bd.max_nkb;
+    a.keep_pad = sel ? sel->keep_pad : nullptr;
+    a.counts = sel ? sel->counts : nullptr;
+    a.alpha = sel ? sel->alpha : 0.f;
+    a.sink_blocks = sel ? sel->sink_blocks : 0;
+    a.local_blocks = sel ? sel->local_blocks : 0;
     a.status = status;
     a.wait_ns = wait_ns;
     tmQ = tmM;                           // not read: the row warps load the queries themselves

@@ -140,15 +140,21 @@ select_count_kernel(const __grid_constant__ BatchDesc bd, SelectArgs a, const fl
     if (lane == 0) counts[row] = cnt;
 }
 
-// Exclusive scan of counts[0..n) into row_ptr[0..n], nnz = row_ptr[n].
+// Exclusive scan of the row counts into row_ptr[0..n], nnz = row_ptr[n]; row
+// k's count is the sum of counts[k * per_row .. k * per_row + per_row).
 __global__ void __launch_bounds__(1024)
-scan_kernel(const int *__restrict__ counts, int n, int *__restrict__ row_ptr, int *__restrict__ nnz) {
+scan_kernel(const int *__restrict__ counts, int n, int per_row, int *__restrict__ row_ptr, int *__restrict__ nnz) {
     __shared__ int warp_tot[32];
     const int tid = threadIdx.x;
     const int per = (n + 1023) / 1024;
     const int b = tid * per, e = min(n, b + per);
+    auto count = [&](int k) {
+        int c = 0;
+        for (int q = 0; q < per_row; ++q) c += counts[(long long)k * per_row + q];
+        return c;
+    };
     int sum = 0;
-    for (int k = b; k < e; ++k) sum += counts[k];
+    for (int k = b; k < e; ++k) sum += count(k);
     // inclusive scan of the per-thread sums
     int lane = tid % 32, w = tid / 32;
     int v = sum;
@@ -172,7 +178,7 @@ scan_kernel(const int *__restrict__ counts, int n, int *__restrict__ row_ptr, in
     int run = v - sum + (w > 0 ? warp_tot[w - 1] : 0);
     for (int k = b; k < e; ++k) {
         row_ptr[k] = run;
-        run += counts[k];
+        run += count(k);
     }
     if (tid == 1023) {
         int total = warp_tot[31];
@@ -209,6 +215,45 @@ select_compact_kernel(const __grid_constant__ BatchDesc bd, SelectArgs a, const 
     }
 }
 
+// fused path: row warp w of the score kernel wrote the kept blocks of segment
+// w of the row at keep_pad[row offset + w * score_segment(I + 1)], and their
+// count at counts8[row * 8 + w]; after the scan, one warp per row joins the
+// segments into col_idx[row_ptr[row]..]
+__global__ void __launch_bounds__(256)
+select_gather_kernel(const __grid_constant__ BatchDesc bd, const int *__restrict__ keep_pad,
+                     const int *__restrict__ counts8, const int *__restrict__ row_ptr, int *__restrict__ col_idx,
+                     long long col_capacity, int *status) {
+    const int row = blockIdx.x * 8 + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= bd.total_rows) return;
+    const int r = req_of_row(bd, row);
+    const ReqDesc &rq = bd.req[r];
+    const int local = row - rq.row_base;
+    const int i = local / bd.h_kv, h = local % bd.h_kv;
+    const int *src = keep_pad + score_row_offset(rq, bd.h_kv, i, h);
+    const int I = rq.start / kBlock + i;
+    const int seg = score_segment(I + 1);
+    const int b = row_ptr[row], n = row_ptr[row + 1] - b;
+    if ((long long)b + n > col_capacity) {
+        if (lane == 0) set_status(status, FP_ERR_INVALID);
+        return;
+    }
+    int pos = b;
+    for (int w = 0; w < 8; ++w) {
+        const int c = __ldg(counts8 + (long long)row * 8 + w);
+        for (int k = lane; k < c; k += 32) col_idx[pos + k] = __ldg(src + w * seg + k);
+        pos += c;
+    }
+}
+
+cudaError_t launch_select_gather(const BatchDesc &bd, const int *keep_pad, const int *counts, int *row_ptr,
+                                 int *col_idx, long long col_capacity, int *nnz, int *status, cudaStream_t st) {
+    const int grid = (bd.total_rows + 7) / 8;
+    scan_kernel<<<1, 1024, 0, st>>>(counts, bd.total_rows, 8, row_ptr, nnz);
+    select_gather_kernel<<<grid, 256, 0, st>>>(bd, keep_pad, counts, row_ptr, col_idx, col_capacity, status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_select(const BatchDesc &bd, float alpha, int sink_blocks, int local_blocks, int rule,
                           int top_k, float top_p, const float *score, int *counts, int *row_ptr, int *col_idx,
                           long long col_capacity, int *nnz, unsigned char *dense_mask, int *status,
@@ -216,7 +261,7 @@ cudaError_t launch_select(const BatchDesc &bd, float alpha, int sink_blocks, int
     SelectArgs a{alpha, sink_blocks, local_blocks, rule, top_k, top_p};
     int grid = (bd.total_rows + 7) / 8;
     select_count_kernel<<<grid, 256, 0, st>>>(bd, a, score, counts, dense_mask);
-    scan_kernel<<<1, 1024, 0, st>>>(counts, bd.total_rows, row_ptr, nnz);
+    scan_kernel<<<1, 1024, 0, st>>>(counts, bd.total_rows, 1, row_ptr, nnz);
     select_compact_kernel<<<grid, 256, 0, st>>>(bd, a, score, row_ptr, col_idx, col_capacity, status);
     return cudaGetLastError();
 }

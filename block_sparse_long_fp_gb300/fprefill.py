@@ -66,6 +66,9 @@ def lib():
             "fp_select_workspace_size": ([P, PP], c_size_t),
             "fp_select": ([P, PP, c_void_p, c_void_p, c_void_p, c_longlong, c_void_p, c_void_p,
                            c_void_p, c_size_t, c_void_p], c_int),
+            "fp_discover_select_workspace_size": ([P, PP], c_size_t),
+            "fp_discover_select": ([P, PP, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_longlong, c_void_p,
+                                    c_void_p, c_size_t, c_void_p], c_int),
             "fp_attn_workspace_size": ([P, PP], c_size_t),
             "fp_attn_kv_splits": ([P, PP], c_int),
             "fp_sparse_attn": ([P, PP, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -159,6 +162,7 @@ class Layer:
         self.kv_splits = int(L.fp_attn_kv_splits(pp, pm))   # split-KV parts of the attention calls
         self.ws_bytes = max(int(L.fp_discover_workspace_size(pp, pm)),
                             int(L.fp_select_workspace_size(pp, pm)),
+                            int(L.fp_discover_select_workspace_size(pp, pm)),
                             int(L.fp_attn_workspace_size(pp, pm)))
         self._ws = None
 
@@ -205,6 +209,24 @@ class Layer:
                                _ptr(nnz), _ptr(dense_mask), _ptr(ws), self.ws_bytes, _stream_handle()),
                "fp_select")
         return row_ptr, col_idx, nnz
+
+    def discover_select(self, k_mean=None, v_mean=None, score=None, row_ptr=None, col_idx=None, nnz=None):
+        """fp_discover_select: block means and the CSR index in one call (the
+        score map only when `score` is given)."""
+        import torch
+        dev = self.q.device
+        shape = (self.key_blocks, self.h_kv, int(self.q.shape[-1]))
+        k_mean = k_mean if k_mean is not None else torch.empty(shape, dtype=torch.float32, device=dev)
+        v_mean = v_mean if v_mean is not None else torch.empty(shape, dtype=torch.float32, device=dev)
+        row_ptr = row_ptr if row_ptr is not None else torch.empty(self.rows + 1, dtype=torch.int32, device=dev)
+        col_idx = col_idx if col_idx is not None else torch.empty(max(1, self.score_size), dtype=torch.int32,
+                                                                  device=dev)
+        nnz = nnz if nnz is not None else torch.empty(1, dtype=torch.int32, device=dev)
+        ws = self.workspace()
+        _check(lib().fp_discover_select(*self._refs(), _ptr(k_mean), _ptr(v_mean), _ptr(score), _ptr(row_ptr),
+                                        _ptr(col_idx), col_idx.numel(), _ptr(nnz), _ptr(ws), self.ws_bytes,
+                                        _stream_handle()), "fp_discover_select")
+        return k_mean, v_mean, row_ptr, col_idx, nnz
 
     def _out(self, out, lse):
         import torch

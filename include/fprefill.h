@@ -194,6 +194,24 @@ fp_status fp_select(const fp_problem *p, const fp_params *prm, const float *scor
                     unsigned char *dense_mask_opt, void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * fp_discover_select -- fp_discover and fp_select in one call
+ * [V1 summary 3.1-3.3 run back to back]
+ *
+ * Same results as fp_discover followed by fp_select with the same params (the
+ * same k_mean / v_mean, score map and CSR index).  With the threshold rule on
+ * rows the tensor-core score kernel takes, that kernel decides each row and
+ * lists its kept blocks itself, so the score map is neither written (unless
+ * score_opt is given) nor read back.
+ *   score_opt (device fp32, fp_score_size() floats, may be NULL).
+ *   row_ptr, col_idx, col_capacity, nnz_dev as fp_select.
+ *   ws: fp_discover_select_workspace_size() bytes.
+ * ------------------------------------------------------------------------- */
+size_t fp_discover_select_workspace_size(const fp_problem *p, const fp_params *prm);
+fp_status fp_discover_select(const fp_problem *p, const fp_params *prm, float *k_mean, float *v_mean,
+                             float *score_opt, int *row_ptr, int *col_idx, long long col_capacity,
+                             int *nnz_dev, void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
  * fp_sparse_attn -- block-sparse attention with block-mean correction
  * [V2 paper reading 4.1 (mean correction), 4.2 (PackGQA, warp
  *  specialisation, FP8), 4.3 (paged KV through the page table)]

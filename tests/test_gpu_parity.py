@@ -219,6 +219,39 @@ def test_topk_topp_on_a_ragged_varlen_batch(select):
     full_parity(spec, select=select)
 
 
+@pytest.mark.parametrize("name,select", [("varlen", None), ("sharp", None), ("e4m3", None),
+                                         ("sharp", dict(select_rule=1, top_k=4))])
+def test_discover_select_equals_the_separate_stages(name, select):
+    """fp_discover_select gives bit for bit what fp_discover + fp_select give:
+    the same means, score map and index (fused with the threshold rule; the
+    separate kernels behind one call for the other rules)."""
+    import torch
+    from block_sparse_long_fp_gb300 import fprefill
+    specs = {
+        "varlen": synth.Spec("varlen-small", [(300, 0), (1000, 0), (256, 512), (1, 128), (640, 0)], 8, 2,
+                             page_size=32, layout="interleaved", n_needles=2, logit_scale=6.0, config_id=93),
+        "sharp": synth.Spec("sharp-8k", [(8192, 0)], 4, 1, page_size=64, layout="shuffled", n_needles=2,
+                            logit_scale=8.0, config_id=1),
+        "e4m3": synth.Spec("e4m3-chunk", [(1024, 2048), (700, 0)], 8, 2, page_size=64, layout="shuffled",
+                           n_needles=2, logit_scale=6.0, dtype="e4m3", config_id=94),
+    }
+    case = synth.make_case(specs[name])
+    layer = fprefill.layer_from_case(case, params=fprefill.default_params(**(select or {})))
+    km, vm, sc = layer.discover()
+    rp, ci, nz = layer.select(sc)
+    score = torch.full_like(sc, float("nan"))
+    km2, vm2, rp2, ci2, nz2 = layer.discover_select(score=score)
+    km3, vm3, rp3, ci3, nz3 = layer.discover_select()
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    n = int(nz.item())
+    assert int(nz2.item()) == n and int(nz3.item()) == n
+    assert torch.equal(km, km2) and torch.equal(vm, vm2)
+    assert torch.equal(sc, score)
+    assert torch.equal(rp, rp2) and torch.equal(rp, rp3)
+    assert torch.equal(ci[:n], ci2[:n]) and torch.equal(ci[:n], ci3[:n])
+
+
 def test_page_table_entry_out_of_range_sets_status():
     """A corrupted page-table entry is caught by the kernels' bounds checks:
     the status word reports it and the run completes."""
