@@ -254,21 +254,28 @@ def selection_ablation(layer, spec, stream):
     rows = torch.arange(0, layer.total_q, 64, device=dense.device)
     ref = dense[rows].float()
     k_mean, v_mean, score = layer.discover()
-    saved = (layer.params.select_rule, layer.params.top_k, layer.params.top_p)
+    saved = (layer.params.select_rule, layer.params.top_k, layer.params.top_p, layer.params.score_mode)
     out = {}
-    rules = [("threshold_alpha_0.1", fprefill.FP_SELECT_THRESHOLD, 0, 0.0),
-             ("top_k_64", fprefill.FP_SELECT_TOPK, 64, 0.0),
-             ("top_p_0.9", fprefill.FP_SELECT_TOPP, 0, 0.9),
-             ("top_p_0.5", fprefill.FP_SELECT_TOPP, 0, 0.5)]
-    for name, rule, k, p in rules:
-        layer.params.select_rule, layer.params.top_k, layer.params.top_p = rule, k, p
+    rules = [("threshold_alpha_0.1", fprefill.FP_SELECT_THRESHOLD, 0, 0.0, fprefill.FP_SCORE_PACKED),
+             ("top_k_64", fprefill.FP_SELECT_TOPK, 64, 0.0, fprefill.FP_SCORE_PACKED),
+             ("top_p_0.9", fprefill.FP_SELECT_TOPP, 0, 0.9, fprefill.FP_SCORE_PACKED),
+             ("top_p_0.5", fprefill.FP_SELECT_TOPP, 0, 0.5, fprefill.FP_SCORE_PACKED),
+             ("head_union_alpha_0.1", fprefill.FP_SELECT_THRESHOLD, 0, 0.0, fprefill.FP_SCORE_HEAD_UNION)]
+    for name, rule, k, p, mode in rules:
+        layer.params.select_rule, layer.params.top_k, layer.params.top_p, layer.params.score_mode = rule, k, p, mode
+        entry = {}
+        if mode != fprefill.FP_SCORE_PACKED:
+            k_mean, v_mean, score = layer.discover()
+            entry["discover_ms"] = round(cuda_time(lambda: layer.discover(k_mean, v_mean, score), 3, stream), 4)
         rp, ci, nnz = layer.select(score)
         o, _ = layer.sparse_attn(rp, ci, k_mean, v_mean, want_lse=False)
         ms = cuda_time(lambda: layer.sparse_attn(rp, ci, k_mean, v_mean, out=o, want_lse=False), 3, stream)
         stats = index_stats(spec, rp.cpu().numpy())
         err = float(torch.linalg.vector_norm(o[rows].float() - ref) / torch.linalg.vector_norm(ref))
-        out[name] = {"density": round(stats["density"], 5), "attn_ms": round(ms, 4), "rel_err_vs_dense": round(err, 5)}
-    layer.params.select_rule, layer.params.top_k, layer.params.top_p = saved
+        entry.update({"density": round(stats["density"], 5), "attn_ms": round(ms, 4),
+                      "rel_err_vs_dense": round(err, 5)})
+        out[name] = entry
+    (layer.params.select_rule, layer.params.top_k, layer.params.top_p, layer.params.score_mode) = saved
     return out
 
 

@@ -31,6 +31,7 @@ fp_status build_desc(const fp_problem *p, const fp_params *prm, BatchDesc *bd) {
     if (prm->select_rule == FP_SELECT_TOPK && prm->top_k < 1) return FP_ERR_INVALID;
     if (prm->select_rule == FP_SELECT_TOPP && !(prm->top_p > 0.f && prm->top_p <= 1.f)) return FP_ERR_INVALID;
     if (prm->select_rule < FP_SELECT_THRESHOLD || prm->select_rule > FP_SELECT_TOPP) return FP_ERR_INVALID;
+    if (prm->score_mode != FP_SCORE_PACKED && prm->score_mode != FP_SCORE_HEAD_UNION) return FP_ERR_INVALID;
     memset(bd, 0, sizeof(*bd));
     bd->batch = p->batch;
     bd->h_q = p->h_q;
@@ -168,6 +169,7 @@ fp_params fp_default_params(void) {
     p.select_rule = FP_SELECT_THRESHOLD;
     p.top_k = 0;
     p.top_p = 0.f;
+    p.score_mode = FP_SCORE_PACKED;
     return p;
 }
 
@@ -207,6 +209,8 @@ fp_status fp_discover(const fp_problem *p, const fp_params *prm, float *k_mean, 
     if (!ws || ws_bytes < fp_discover_workspace_size(p, prm)) return FP_ERR_WORKSPACE;
     const bool tc = use_score_tc(p, bd);
     if (!tc && score_smem_bytes(bd.max_nkb) > 227 * 1024) return FP_ERR_UNSUPPORTED;
+    const bool head_union = prm->score_mode == FP_SCORE_HEAD_UNION;
+    if (head_union && !tc) return FP_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     const bool fp8 = p->dtype == FP_E4M3;
     if (bd.total_kb > 0 &&
@@ -222,7 +226,7 @@ fp_status fp_discover(const fp_problem *p, const fp_params *prm, float *k_mean, 
             e = launch_score_tc(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean,
                                 softmax_scale_of(prm, p->d), score,
                                 reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + kWsHeaderBytes),
-                                status_ptr(ws), g_wait_ns, st);
+                                status_ptr(ws), g_wait_ns, st, nullptr, head_union);
         if (e != cudaSuccess) return FP_ERR_CUDA;
     }
     return FP_OK;
@@ -274,6 +278,8 @@ fp_status fp_discover_select(const fp_problem *p, const fp_params *prm, float *k
     if (!ws || ws_bytes < fp_discover_select_workspace_size(p, prm)) return FP_ERR_WORKSPACE;
     const bool tc = use_score_tc(p, bd);
     if (!tc && score_smem_bytes(bd.max_nkb) > 227 * 1024) return FP_ERR_UNSUPPORTED;
+    const bool head_union = prm->score_mode == FP_SCORE_HEAD_UNION;
+    if (head_union && !tc) return FP_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     const bool fp8 = p->dtype == FP_E4M3;
     char *w = static_cast<char *>(ws);
@@ -296,7 +302,7 @@ fp_status fp_discover_select(const fp_problem *p, const fp_params *prm, float *k
     __nv_bfloat16 *terms = reinterpret_cast<__nv_bfloat16 *>(w + kWsHeaderBytes);
     const float scale = softmax_scale_of(prm, p->d);
     cudaError_t e;
-    if (tc && prm->select_rule == FP_SELECT_THRESHOLD) {
+    if (tc && prm->select_rule == FP_SELECT_THRESHOLD && !head_union) {
         // one pass: the score kernel decides each row and lists its kept blocks
         ScoreSelect sel{keep_pad, counts, prm->alpha, sink_blocks, local_blocks};
         e = launch_score_tc(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean, scale, score_opt,
@@ -307,7 +313,7 @@ fp_status fp_discover_select(const fp_problem *p, const fp_params *prm, float *k
         // the separate stages, with the score map in the workspace when none is given
         float *sc = score_opt ? score_opt : reinterpret_cast<float *>(keep_pad);
         e = tc ? launch_score_tc(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean, scale, sc,
-                                 terms, status_ptr(ws), g_wait_ns, st)
+                                 terms, status_ptr(ws), g_wait_ns, st, nullptr, head_union)
                : launch_score(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean, scale, sc, st);
         if (e == cudaSuccess)
             e = launch_select(bd, prm->alpha, sink_blocks, local_blocks, prm->select_rule, prm->top_k, prm->top_p, sc,

@@ -31,7 +31,7 @@ struct ScoreSelect {
 cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
                             long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
                             float *score, __nv_bfloat16 *terms, int *status, unsigned long long wait_ns,
-                            cudaStream_t st, const ScoreSelect *sel = nullptr);
+                            cudaStream_t st, const ScoreSelect *sel = nullptr, bool head_union = false);
 cudaError_t launch_select_gather(const BatchDesc &bd, const int *keep_pad, const int *counts, int *row_ptr,
                                  int *col_idx, long long col_capacity, int *nnz, int *status, cudaStream_t st);
 

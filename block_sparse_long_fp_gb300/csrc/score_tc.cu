@@ -65,7 +65,7 @@ struct ScoreCfg {
     static constexpr int B_QF = 0, B_QE = 4, B_SF = 8, B_SE = 8 + kStages, B_TF = 8 + 2 * kStages;
     static constexpr int B_TE = B_TF + 4, B_N = B_TE + 4;
     static_assert(kTmemQ + 256 <= 512, "TMEM budget");
-    static_assert(B_N * 8 + 64 <= 512, "control block");
+    static_assert(B_N * 8 + 128 <= 512, "control block");
     static size_t smem_bytes(int max_nkb) { return (size_t)kSmAcc + 8 * sizeof(float) * max_nkb + 1024; }
 };
 
@@ -85,6 +85,7 @@ struct ScoreTcArgs {
     float alpha;
     int sink_blocks;
     int local_blocks;
+    int head_union;           // FP_SCORE_HEAD_UNION: each head normalised alone, max over heads
     int *status;
     unsigned long long wait_ns;
 };
@@ -176,6 +177,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kSmCtl + B_N * 8 + 4);
     float *red = reinterpret_cast<float *>(smem + kSmCtl + B_N * 8 + 16);   // [8]
     unsigned *sync_ctr = reinterpret_cast<unsigned *>(smem + kSmCtl + B_N * 8 + 48);
+    float *red_h = reinterpret_cast<float *>(smem + kSmCtl + B_N * 8 + 64);    // [16]
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t sbase = smem_u32(smem);
@@ -343,14 +345,17 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
         };
         if (w < g) ok = put_queries(0);
         for (int pr = 0; pr < npairs && ok; ++pr) {
-            if (2 * pr + w >= g) break;
-            const int hq = h * g + 2 * pr + w;
+            // a slot without a head in this pair (odd g, last pair) has no passes;
+            // under the union of heads it still takes part in the pair's syncs
+            const bool has_head = 2 * pr + w < g;
+            if (!has_head && !a.head_union) break;
+            const int hq = h * g + 2 * pr + (has_head ? w : 0);
             const bool next = 2 * (pr + 1) + w < g;       // this slot has a head in the next pair
             if (next) prefetch_queries(pr + 1);
             const float c2 = kFp8 ? a.scale_log2 * __ldg(a.q_scale + hq) : a.scale_log2;
             float m = -INFINITY;
             float mc2 = 0.f;
-            for (int pass = 0; pass < 2 && ok; ++pass) {
+            for (int pass = 0; pass < 2 && ok && has_head; ++pass) {
                 if (pass == 1) {
                     mc2 = !row_valid ? INFINITY : (m == -INFINITY ? 0.f : m * c2);
                     // the next pair's queries go into the other buffer while this
@@ -413,10 +418,63 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                     }
                 }
             }
+            if (a.head_union && ok) {
+                // union of heads: this pair's two heads are complete in the
+                // accumulators (four warps each).  Each head's row is normalised by
+                // its own maximum and folded into the output row by maximum; the
+                // accumulators are cleared for the next pair.
+                const int t = threadIdx.x - 128;
+                const int st = a.acc_stride;
+                auto head_sum = [&](int ww, int J) {
+                    const float *b0 = acc + ww * 4 * st;
+                    return (b0[J] + b0[st + J]) + (b0[2 * st + J] + b0[3 * st + J]);
+                };
+                const bool h1 = 2 * pr + 1 < g;
+                ok = rows_sync(sync_ctr, gen, lane, abort_flag, a.status, a.wait_ns);
+                if (!ok) break;
+                float m0 = 0.f, m1 = 0.f;
+                for (int J = t; J < ncol; J += 256) {
+                    m0 = fmaxf(m0, head_sum(0, J));
+                    if (h1) m1 = fmaxf(m1, head_sum(1, J));
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+                }
+                if (lane == 0) {
+                    red_h[warp - 4] = m0;
+                    red_h[8 + warp - 4] = m1;
+                }
+                ok = rows_sync(sync_ctr, gen, lane, abort_flag, a.status, a.wait_ns);
+                if (!ok) break;
+                float M0 = 0.f, M1 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    M0 = fmaxf(M0, red_h[k]);
+                    M1 = fmaxf(M1, red_h[8 + k]);
+                }
+                const float i0 = 1.f / M0, i1 = h1 ? 1.f / M1 : 0.f;
+                for (int J = t; J < ncol; J += 256) {
+                    const float v0 = head_sum(0, J);
+                    float u = v0 == M0 ? 1.f : v0 * i0;
+                    if (h1) {
+                        const float v1 = head_sum(1, J);
+                        u = fmaxf(u, v1 == M1 ? 1.f : v1 * i1);
+                    }
+                    if (pr > 0) u = fmaxf(u, out[J]);
+                    out[J] = u;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) acc[k * st + J] = 0.f;
+                }
+                ok = rows_sync(sync_ctr, gen, lane, abort_flag, a.status, a.wait_ns);
+                if (!ok) break;
+            }
         }
         // S' = the eight warps' sums (fixed order); re-normalise by its maximum
-        if (ok) ok = rows_sync(sync_ctr, gen, lane, abort_flag, a.status, a.wait_ns);
-        if (ok) {
+        // (the union of heads has written its row pair by pair)
+        if (ok && !a.head_union) ok = rows_sync(sync_ctr, gen, lane, abort_flag, a.status, a.wait_ns);
+        if (ok && !a.head_union) {
             const int t = threadIdx.x - 128;
             const int st = a.acc_stride;
             auto colsum = [&](int J) {
@@ -532,7 +590,7 @@ size_t score_tc_smem_bytes(int max_nkb) {
 cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
                             long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
                             float *score, __nv_bfloat16 *terms, int *status, unsigned long long wait_ns,
-                            cudaStream_t st, const ScoreSelect *sel) {
+                            cudaStream_t st, const ScoreSelect *sel, bool head_union) {
     const int rows_pad = score_tc_rows_pad(bd);
     const long long n = (long long)bd.total_kb * bd.h_kv * kHeadDim;
     const long long n_pad = (long long)rows_pad * bd.h_kv * kHeadDim;
@@ -559,6 +617,7 @@ cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long l
     a.alpha = sel ? sel->alpha : 0.f;
     a.sink_blocks = sel ? sel->sink_blocks : 0;
     a.local_blocks = sel ? sel->local_blocks : 0;
+    a.head_union = head_union ? 1 : 0;
     a.status = status;
     a.wait_ns = wait_ns;
     tmQ = tmM;                           // not read: the row warps load the queries themselves

@@ -20,12 +20,14 @@ FP_OK, FP_ERR_INVALID, FP_ERR_UNSUPPORTED, FP_ERR_WORKSPACE, FP_ERR_CUDA, FP_ERR
 FP_BF16, FP_E4M3 = 0, 1
 FP_MAX_BATCH = 128
 FP_SELECT_THRESHOLD, FP_SELECT_TOPK, FP_SELECT_TOPP = 0, 1, 2
+FP_SCORE_PACKED, FP_SCORE_HEAD_UNION = 0, 1
 
 
 class FpParams(Structure):
     _fields_ = [("block", c_int), ("sink_tokens", c_int), ("local_tokens", c_int),
                 ("alpha", c_float), ("softmax_scale", c_float), ("mean_correction", c_int),
-                ("kv_splits", c_int), ("select_rule", c_int), ("top_k", c_int), ("top_p", c_float)]
+                ("kv_splits", c_int), ("select_rule", c_int), ("top_k", c_int), ("top_p", c_float),
+                ("score_mode", c_int)]
 
 
 class FpProblem(Structure):

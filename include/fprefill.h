@@ -103,7 +103,15 @@ typedef struct {
                              kept under every rule */
     int top_k;            /* FP_SELECT_TOPK: blocks kept per row (>= 1) */
     float top_p;          /* FP_SELECT_TOPP: share of the row's score mass kept, (0, 1] */
+    int score_mode;       /* fp_discover: FP_SCORE_PACKED or FP_SCORE_HEAD_UNION */
 } fp_params;
+
+/* Score modes of fp_discover.  PACKED is the reading of the V1 summary 3.1
+ * with PackGQA (the g heads x B queries of a group are one set of packed
+ * rows); HEAD_UNION is the alternative: each query head's row is normalised
+ * on its own and the row keeps the maximum over the group's heads, so the
+ * threshold keeps the union of the heads' own selections. */
+typedef enum { FP_SCORE_PACKED = 0, FP_SCORE_HEAD_UNION = 1 } fp_score_mode;
 
 /* Selection rules of fp_select.  THRESHOLD is the method's rule [V1 summary
  * 3.2]; TOPK and TOPP are the alternatives it is compared with [V1 summary
@@ -165,6 +173,9 @@ long long fp_total_q(const fp_problem *p);                               /* cu_s
  *     (g = h_q / h_kv heads of the group x the block's queries) contributes
  *     exp(s_J - max_J' s_J') to S'[J], s_J = scale * q . k_mean_J for J <= I;
  *     Score[I,J] = S'[J] / max_J' S'[J'] (so each row peaks at exactly 1).
+ *     FP_SCORE_HEAD_UNION: the same per query head (its B queries alone),
+ *     and Score[I,J] = max over the group's heads of those rows (still
+ *     peaking at 1); rows over 2647 key blocks: FP_ERR_UNSUPPORTED.
  *   ws: fp_discover_workspace_size() bytes (status header only).
  * ------------------------------------------------------------------------- */
 size_t fp_discover_workspace_size(const fp_problem *p, const fp_params *prm);

@@ -10,6 +10,8 @@ Parity status of each function (what pins it; see tests/test_oracle_pins.py):
   score_rows   pinned: hand-derived closed form (tests/golden/score_tiny.json),
                per-query shift invariance, head/query permutation invariance,
                row maximum exactly 1.
+  score_rows_head_union   pinned: g = 1 reduces it to score_rows, head-order
+               invariance, each head's own normalised row bounded by it, max 1.
   select_row   pinned: brute-force rule check, sink/local/causal invariants;
                top-k / top-p: count, dominance, tie order, minimal mass, limits.
   attn_rows    pinned: alpha=0 equals direct dense causal softmax; exact mean
@@ -150,6 +152,23 @@ def score_rows(q, start, hkv, B, scale, kbar, rows):
     return [out[o:o + n] for o, n in zip(off, lens)]
 
 
+def score_rows_head_union(q, start, hkv, B, scale, kbar, rows):
+    """The union-of-heads reading of the score rows (V1 summary 3.1 applied to
+    each query head alone): for row (i_local, h), each query head h' of the
+    group scores the block with its own B queries and its row is normalised to
+    a maximum of 1; the row is the maximum over the group's heads."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    lq, hq, d = q.shape
+    g = hq // hkv
+    out = []
+    for row in rows:
+        il, h = divmod(int(row), hkv)
+        per_head = [score_rows(q[:, hh:hh + 1, :], start, 1, B, scale, kbar[:, h:h + 1, :], [il])[0]
+                    for hh in range(h * g, (h + 1) * g)]
+        out.append(np.max(np.stack(per_head), axis=0))
+    return out
+
+
 def select_row(score_row: np.ndarray, I: int, alpha: float, B: int, sink: int, local: int, rule: int = 0,
                top_k: int = 0, top_p: float = 0.0):
     """keep / flag masks of one score row: rule 0 the max threshold, 1 top-k,
@@ -221,7 +240,7 @@ def csr_from_keep(keep_rows):
 
 
 def discover_and_select(case, B=128, sink=256, local=512, alpha=0.1, scale=None,
-                        requests_subset=None, row_subset=None, rule=0, top_k=0, top_p=0.0):
+                        requests_subset=None, row_subset=None, rule=0, top_k=0, top_p=0.0, head_union=False):
     """Steps 1-3 for every request (or a subset): block means, score rows,
     keep / flag masks.  Returns a dict with per-request results."""
     spec = case.spec
@@ -236,7 +255,7 @@ def discover_and_select(case, B=128, sink=256, local=512, alpha=0.1, scale=None,
         kbar, vbar = pool(k, B), pool(v, B)
         nqb = -(-lq // B)
         rows = np.arange(nqb * hkv) if row_subset is None else np.asarray(row_subset(r, nqb, hkv))
-        srows = score_rows(q, start, hkv, B, scale, kbar, rows)
+        srows = (score_rows_head_union if head_union else score_rows)(q, start, hkv, B, scale, kbar, rows)
         keep = np.zeros((nqb, hkv, kbar.shape[0]), dtype=np.uint8)
         flag = np.zeros((nqb, hkv, kbar.shape[0]), dtype=np.uint8)
         have = np.zeros((nqb, hkv), dtype=bool)

@@ -13,14 +13,16 @@ FP8_LSE_ABS = 2e-2
 SCORE_ABS = 2e-6          # scores lie in (0, 1]; fp32 evaluation error is ~1e-7
 
 
-def gpu_stage_outputs(case, alpha=0.1, mean_corr=True, dense=False, kv_splits=0, select=None):
+def gpu_stage_outputs(case, alpha=0.1, mean_corr=True, dense=False, kv_splits=0, select=None, attention=True):
     import torch
     from block_sparse_long_fp_gb300 import fprefill
     prm = fprefill.default_params(alpha=alpha, mean_correction=int(mean_corr), kv_splits=kv_splits, **(select or {}))
     layer = fprefill.layer_from_case(case, params=prm)
     k_mean, v_mean, score = layer.discover()
     row_ptr, col_idx, nnz = layer.select(score)
-    if dense:
+    if not attention:
+        out = lse = None
+    elif dense:
         out, lse = layer.dense_attn()
     else:
         out, lse = layer.sparse_attn(row_ptr, col_idx, k_mean, v_mean)
@@ -29,7 +31,8 @@ def gpu_stage_outputs(case, alpha=0.1, mean_corr=True, dense=False, kv_splits=0,
     return dict(layer=layer, k_mean=k_mean.cpu().numpy(), v_mean=v_mean.cpu().numpy(),
                 score=score.cpu().numpy(), row_ptr=row_ptr.cpu().numpy(),
                 col_idx=col_idx.cpu().numpy(), nnz=int(nnz.item()),
-                out=out.float().cpu().numpy(), lse=lse.cpu().numpy(), status=st)
+                out=None if out is None else out.float().cpu().numpy(),
+                lse=None if lse is None else lse.cpu().numpy(), status=st)
 
 
 def check_pool(case, g, ref):

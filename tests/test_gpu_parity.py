@@ -29,7 +29,7 @@ def full_parity(spec, alpha=0.1, mean_corr=True, rows_per_request=None, max_abs=
     case = synth.make_case(spec)
     sel = select or {}
     ref = oracle.discover_and_select(case, alpha=alpha, rule=sel.get("select_rule", 0), top_k=sel.get("top_k", 0),
-                                     top_p=sel.get("top_p", 0.0))
+                                     top_p=sel.get("top_p", 0.0), head_union=sel.get("score_mode", 0) == 1)
     g = gpu_stage_outputs(case, alpha=alpha, mean_corr=mean_corr, select=select)
     assert g["status"] == 0
     check_pool(case, g, ref)
@@ -250,6 +250,42 @@ def test_discover_select_equals_the_separate_stages(name, select):
     assert torch.equal(sc, score)
     assert torch.equal(rp, rp2) and torch.equal(rp, rp3)
     assert torch.equal(ci[:n], ci2[:n]) and torch.equal(ci[:n], ci3[:n])
+
+
+@pytest.mark.parametrize("name", ["varlen", "sharp", "e4m3"])
+def test_union_of_heads_scores_selection_and_attention(name):
+    """FP_SCORE_HEAD_UNION (each query head scored alone, the row keeps the
+    maximum over the group): scores within 2e-6, the index exact outside the
+    flagged band, the attention on it within the bounds."""
+    from parity_util import FP8_LSE_ABS, FP8_MAX_ABS
+    specs = {
+        "varlen": synth.Spec("varlen-small", [(300, 0), (1000, 0), (256, 512), (1, 128), (640, 0)], 8, 2,
+                             page_size=32, layout="interleaved", n_needles=2, logit_scale=6.0, config_id=95),
+        "sharp": synth.Spec("sharp-8k", [(8192, 0)], 4, 1, page_size=64, layout="shuffled", n_needles=2,
+                            logit_scale=8.0, config_id=1),
+        "e4m3": synth.Spec("e4m3-chunk", [(1024, 2048), (700, 0)], 8, 2, page_size=64, layout="shuffled",
+                           n_needles=2, logit_scale=6.0, dtype="e4m3", config_id=96),
+    }
+    fp8 = name == "e4m3"
+    r = full_parity(specs[name], rows_per_request=1500, select=dict(score_mode=1),
+                    max_abs=FP8_MAX_ABS if fp8 else None, mean_abs=6e-3 if fp8 else None,
+                    lse_abs=FP8_LSE_ABS if fp8 else 2e-2)
+    if name == "sharp":
+        packed = full_parity(specs[name], rows_per_request=200)
+        assert r["density"] >= packed["density"]   # every head's own blocks: a larger union
+
+
+def test_union_of_heads_with_an_odd_group():
+    """Three query heads per kv head (the last pair has one head): scores and
+    index only (the attention kernel takes head pairs)."""
+    import oracle
+    spec = synth.Spec("odd-group", [(700, 0), (300, 256)], 6, 2, page_size=64, layout="shuffled", n_needles=1,
+                      logit_scale=6.0, config_id=97)
+    case = synth.make_case(spec)
+    ref = oracle.discover_and_select(case, head_union=True)
+    g = gpu_stage_outputs(case, select=dict(score_mode=1), attention=False)
+    assert g["status"] == 0
+    check_scores_and_index(case, g, ref)
 
 
 def test_page_table_entry_out_of_range_sets_status():

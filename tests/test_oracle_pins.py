@@ -156,6 +156,37 @@ def test_score_invariant_to_query_and_head_permutation(oracle_mod):
     np.testing.assert_allclose(got, base, rtol=1e-13)
 
 
+def test_head_union_scores(oracle_mod):
+    """The union-of-heads score reading: with one head per group it is the
+    packed score; it does not depend on the order of the group's heads; every
+    head's own normalised row lies under it and touches it at its maximum;
+    each row peaks at exactly 1."""
+    rng = np.random.default_rng(14)
+    B, start, hkv, g, d = 16, 32, 2, 3, 8
+    q = rng.normal(size=(70, hkv * g, d))
+    k = rng.normal(size=(start + 70, hkv, d))
+    kbar = oracle_mod.pool(k, B)
+    nqb = -(-70 // B)
+    rows = list(range(nqb * hkv))
+    union = oracle_mod.score_rows_head_union(q, start, hkv, B, 0.3, kbar, rows)
+    # g = 1: the packed score of the single head
+    for hh in range(hkv * g):
+        h = hh // g
+        one = oracle_mod.score_rows_head_union(q[:, hh:hh + 1], start, 1, B, 0.3, kbar[:, h:h + 1], range(nqb))
+        packed = oracle_mod.score_rows(q[:, hh:hh + 1], start, 1, B, 0.3, kbar[:, h:h + 1], range(nqb))
+        for a_, b_ in zip(one, packed):
+            np.testing.assert_array_equal(a_, b_)
+    perm = np.concatenate([h * g + rng.permutation(g) for h in range(hkv)])
+    union_p = oracle_mod.score_rows_head_union(q[:, perm], start, hkv, B, 0.3, kbar, rows)
+    for r, (u, up) in enumerate(zip(union, union_p)):
+        np.testing.assert_array_equal(u, up)
+        assert u.max() == 1.0
+        il, h = divmod(r, hkv)
+        for hh in range(h * g, (h + 1) * g):
+            own = oracle_mod.score_rows(q[:, hh:hh + 1], start, 1, B, 0.3, kbar[:, h:h + 1], [il])[0]
+            assert np.all(own <= u) and u[np.argmax(own)] == 1.0
+
+
 # ----------------------------------------------------------------------------
 # selection
 # ----------------------------------------------------------------------------
