@@ -283,7 +283,8 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         const int tok = J * kBlock + (lane % nsub) * rpb;
                         const int lp = tok / a.page_size;
                         const int npages_req = (rq.lk + a.page_size - 1) / a.page_size;
-                        if (tok < rq.lk && lp < npages_req) {
+                        if (J < 0 || J > U.I) set_status(a.status, FP_ERR_DEVICE_BOUNDS);   // not a block of the row
+                        else if (tok < rq.lk && lp < npages_req) {
                             const int pg = __ldg(a.block_table + (long long)U.r * a.max_pages + lp);
                             if (pg >= 0 && pg < a.num_pages) z = pg * a.page_size + tok % a.page_size;
                             else set_status(a.status, FP_ERR_DEVICE_BOUNDS);
@@ -347,7 +348,12 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                             const int tok = J * kBlock + (lane % nsub) * rpb;
                             const int lp = tok / a.page_size;
                             off = tok % a.page_size;
-                            pg = (tok < rq.lk && lp < npages_req) ? __ldg(bt + lp) : -1;
+                            if (J < 0 || J > U.I) {               // not a block of the row: zero fill
+                                set_status(a.status, FP_ERR_DEVICE_BOUNDS);
+                                pg = -1;
+                            } else {
+                                pg = (tok < rq.lk && lp < npages_req) ? __ldg(bt + lp) : -1;
+                            }
                         }
                     };
                     // row of the paged pool a looked-up box starts at

@@ -79,7 +79,8 @@ typedef enum {
     FP_ERR_UNSUPPORTED = 2,    /* a shape or option this build does not implement */
     FP_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required */
     FP_ERR_CUDA = 4,           /* a CUDA runtime call failed (launch, copy) */
-    FP_ERR_DEVICE_BOUNDS = 5,  /* device status: a page-table entry outside [0, num_pages) */
+    FP_ERR_DEVICE_BOUNDS = 5,  /* device status: a page-table entry outside [0, num_pages), or an
+                                  index entry J outside [0, I] (its tile is read as zeros) */
     FP_ERR_TIMEOUT = 6         /* device status: a bounded wait inside a kernel gave up */
 } fp_status;
 

@@ -303,6 +303,28 @@ def test_page_table_entry_out_of_range_sets_status():
     assert layer.device_status() == fprefill.FP_ERR_DEVICE_BOUNDS
 
 
+def test_index_entry_out_of_range_sets_status():
+    """Index entries outside [0, I] (a negative block, a block after the
+    diagonal) are caught before any page-table read: the status word reports
+    them and the run completes."""
+    import torch
+    from block_sparse_long_fp_gb300 import fprefill
+    spec = synth.Spec("bad-index", [(512, 0)], 4, 2, page_size=64, layout="contiguous", config_id=74)
+    case = synth.make_case(spec)
+    layer = fprefill.layer_from_case(case)
+    k_mean, v_mean, score = layer.discover()
+    row_ptr, col_idx, nnz = layer.select(score)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    rp = row_ptr.cpu().numpy()
+    ci = col_idx.clone()
+    ci[int(rp[0])] = -1                        # row (I = 0, h = 0)
+    ci[int(rp[2 * spec.h_kv + 1])] = 3         # row (I = 2, h = 1): its first entry becomes J = 3 > I
+    layer.sparse_attn(row_ptr, ci, k_mean, v_mean)
+    torch.cuda.synchronize()
+    assert layer.device_status() == fprefill.FP_ERR_DEVICE_BOUNDS
+
+
 @pytest.mark.slow
 def test_llama8b_32k_sampled():
     """Workload 2 (32K, 32/8 heads, shuffled 64-token pages): every pooled
