@@ -421,12 +421,17 @@ const char *fp_status_string(fp_status s) {
         case FP_ERR_UNSUPPORTED: return "unsupported shape or option";
         case FP_ERR_WORKSPACE: return "workspace missing or too small";
         case FP_ERR_CUDA: return "CUDA runtime error";
-        case FP_ERR_DEVICE_BOUNDS: return "page-table entry out of range (device)";
+        case FP_ERR_DEVICE_BOUNDS: return "page-table or index entry out of range (device)";
         case FP_ERR_TIMEOUT: return "bounded wait timed out (device)";
     }
     return "unknown status";
 }
 
 void fp_set_wait_limit_ns(unsigned long long ns) { g_wait_ns = ns ? ns : 200000000ull; }
+
+fp_status fp_check_wait_timeout(void *ws, unsigned long long limit_ns, void *stream) {
+    if (!ws || limit_ns == 0 || limit_ns > 10000000000ull) return FP_ERR_INVALID;
+    return launch_wait_timeout(status_ptr(ws), limit_ns, (cudaStream_t)stream) == cudaSuccess ? FP_OK : FP_ERR_CUDA;
+}
 
 }  // extern "C"

@@ -61,8 +61,9 @@ constexpr int kSmemCtl = 6 * kTileBytes;                   // 192 KB
 constexpr int kBitmapWords = FP_MAX_KEY_BLOCKS / 32;
 constexpr int kMaxCorrTiles = FP_MAX_KEY_BLOCKS / kBlock;
 
+// BAR_DR: the MMA thread's drain before the CTA leaves
 enum { BAR_Q = 0, BAR_QE = 1, BAR_KF = 2, BAR_KE = 4, BAR_VF = 6, BAR_VE = 8, BAR_SF = 10, BAR_PF = 12,
-       BAR_OF = 14, BAR_MF = 16, BAR_ME = 18, NUM_BARS = 20 };
+       BAR_OF = 14, BAR_MF = 16, BAR_ME = 18, BAR_DR = 20, NUM_BARS = 21 };
 // arrivals on a metadata-empty barrier: the TMA thread, the MMA thread and
 // one lane of each of the eight softmax warps
 constexpr int kMetaConsumers = 10;
@@ -322,6 +323,9 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             const int oob = a.num_pages * a.page_size;                     // zero-filled rows
             uint32_t it = 0;
             int kq = 0;
+            // for the drain after an abort (lane 0): the Q phase armed last (-1:
+            // none), and the tile (0: K, 1: V) whose slot wait gave up, if one did
+            int q_ph = -1, fail_op = -1;
             for (int k = 0;; ++k) {
                 const int b = k & 1;
                 const UnitMeta &M = meta[b];
@@ -371,6 +375,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         if (kq > 0 && !mbar_wait(bar(BAR_QE), (kq - 1) & 1, abort_flag, a.status, a.wait_ns)) good = false;
                         if (good) {
                             const int q_row0 = rq.q_off + U.il * kBlock;
+                            q_ph = kq & 1;
                             mbar_expect_tx(bar(BAR_Q), 2 * kT);
                             for (int t = 0; t < 2; ++t)
                                 for (int hf = 0; hf < kNH; ++hf)
@@ -405,6 +410,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                                 if (it >= 2 && !mbar_wait(bar(op == 0 ? BAR_KE + s : BAR_VE + s), ph ^ 1, abort_flag,
                                                           a.status, a.wait_ns)) {
                                     good = false;
+                                    fail_op = op;
                                     break;
                                 }
                                 const uint32_t dst = sbase + (op == 0 ? kSmemK : kSmemV) + s * kTileBytes;
@@ -435,6 +441,19 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 }
                 __syncwarp();                               // the warp's reads of the metadata are done
                 if (lane == 0) mbar_arrive(bar(BAR_ME + b));
+            }
+            // after an abort, the copies armed last land before the CTA leaves
+            // (otherwise every copy has been consumed already)
+            if (lane == 0 && *abort_flag) {
+                if (q_ph >= 0) mbar_wait_drain(bar(BAR_Q), q_ph);
+                // items before `it` were armed in full, except the one whose slot
+                // wait gave up: its K only when the V wait was the one that gave up
+                const int nk = fail_op == 0 ? (int)it - 1 : (int)it;
+                const int nv = fail_op >= 0 ? (int)it - 1 : (int)it;
+                for (int i = nk - 2; i < nk; ++i)
+                    if (i >= 0) mbar_wait_drain(bar(BAR_KF + (i & 1)), (i >> 1) & 1);
+                for (int i = nv - 2; i < nv; ++i)
+                    if (i >= 0) mbar_wait_drain(bar(BAR_VF + (i & 1)), (i >> 1) & 1);
             }
         } else if (warp == 1 && lane == 0) {
             // ================= MMA issuer =================
@@ -534,6 +553,10 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 }
                 if (!good) break;
                 ++kq;
+            }
+            if (*abort_flag) {                         // after an abort, every MMA issued is done
+                tc_commit(bar(BAR_DR));                // before the CTA leaves
+                mbar_wait_drain(bar(BAR_DR), 0);
             }
         }
     } else {
@@ -1055,6 +1078,24 @@ static bool make_map(CUtensorMap *m, const void *base, long long n1, long long n
 }
 
 int attn_smem_bytes() { return kSmemAttn; }
+
+// The failure path of the bounded waits, without a fault: one thread waits on
+// an mbarrier that nothing arrives on, through the same wait the kernels use,
+// and records FP_ERR_TIMEOUT when the limit runs out.
+__global__ void wait_timeout_kernel(int *status, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bar), 1);
+        fence_barrier_init();
+        mbar_wait(smem_u32(&bar), 0, &abort_flag, status, limit_ns);
+    }
+}
+cudaError_t launch_wait_timeout(int *status, unsigned long long limit_ns, cudaStream_t st) {
+    wait_timeout_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+    return cudaGetLastError();
+}
 
 // returns 0 on success, otherwise an fp_status
 int launch_attn(const AttnLaunch &L, cudaStream_t st) {

@@ -63,4 +63,5 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st);
 // rows of the bf16 block-mean copies: at least one full 128-row TMA box
 inline int mean_rows(const BatchDesc &bd) { return bd.total_kb > kBlock ? bd.total_kb : kBlock; }
 int attn_smem_bytes();
+cudaError_t launch_wait_timeout(int *status, unsigned long long limit_ns, cudaStream_t st);
 }  // namespace fp

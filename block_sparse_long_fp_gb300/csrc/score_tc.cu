@@ -63,7 +63,7 @@ struct ScoreCfg {
     // barriers: Q full/empty per (buffer, head slot), stage full/empty, TMEM
     // full/empty per (head slot, S buffer)
     static constexpr int B_QF = 0, B_QE = 4, B_SF = 8, B_SE = 8 + kStages, B_TF = 8 + 2 * kStages;
-    static constexpr int B_TE = B_TF + 4, B_N = B_TE + 4;
+    static constexpr int B_TE = B_TF + 4, B_DR = B_TE + 4, B_N = B_DR + 1;   // B_DR: the MMAs' drain
     static_assert(kTmemQ + 256 <= 512, "TMEM budget");
     static_assert(B_N * 8 + 128 <= 512, "control block");
     static size_t smem_bytes(int max_nkb) { return (size_t)kSmAcc + 8 * sizeof(float) * max_nkb + 1024; }
@@ -168,7 +168,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
     constexpr int kStageBytes = Cfg::kStageBytes, kStages = Cfg::kStages, kSmStage = Cfg::kSmStage;
     constexpr int kSmCtl = Cfg::kSmCtl, kSmAcc = Cfg::kSmAcc, kTmemQ = Cfg::kTmemQ;
     constexpr int B_QF = Cfg::B_QF, B_QE = Cfg::B_QE, B_SF = Cfg::B_SF, B_SE = Cfg::B_SE;
-    constexpr int B_TF = Cfg::B_TF, B_TE = Cfg::B_TE, B_N = Cfg::B_N;
+    constexpr int B_TF = Cfg::B_TF, B_TE = Cfg::B_TE, B_DR = Cfg::B_DR, B_N = Cfg::B_N;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *acc = reinterpret_cast<float *>(smem + kSmAcc);              // [4 warps][acc_stride]
@@ -235,7 +235,12 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                                         t * a.rows_pad + rq.kb_base + c * kChunk);
                 }
             }
-        producer_done:;
+        producer_done:
+            // after an abort, the copies of the last stages armed land before the
+            // CTA leaves (otherwise the MMAs have consumed every stage already)
+            if (*abort_flag)
+                for (int j = step > kStages ? step - kStages : 0; j < step; ++j)
+                    mbar_wait_drain(bar(B_SF + j % kStages), (j / kStages) & 1);
         } else if (warp == 1 && lane == 0) {
             // ================= MMA issuer =================
             constexpr uint32_t idS = idesc_bf16(128, kChunk, false);
@@ -275,7 +280,11 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                 }
                 for (int w = 0; w < nw; ++w) tc_commit(bar(B_QE + 2 * qb + w));
             }
-        mma_done:;
+        mma_done:
+            if (*abort_flag) {                      // after an abort, every MMA issued is done
+                tc_commit(bar(B_DR));               // before the CTA leaves
+                mbar_wait_drain(bar(B_DR), 0);
+            }
         }
     } else {
         // ================= row warpgroups: one head each, one query row per thread =================

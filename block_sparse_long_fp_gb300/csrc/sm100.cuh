@@ -66,6 +66,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Wait for a phase that work already in flight will complete (TMA copies or
+// MMAs issued before the CTA stopped), so that a CTA leaving after an abort
+// does not leave copies landing in its shared memory or MMAs writing its
+// TMEM.  Bounded, and independent of the abort flag.
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0 && global_ns() - t0 > kDrainLimitNs) return false;
+    }
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

@@ -82,6 +82,7 @@ def lib():
             "fp_device_status": ([c_void_p, c_void_p, POINTER(c_int)], c_int),
             "fp_status_string": ([c_int], ctypes.c_char_p),
             "fp_set_wait_limit_ns": ([c_uint64], None),
+            "fp_check_wait_timeout": ([c_void_p, c_uint64, c_void_p], c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -178,6 +179,14 @@ class Layer:
             self._ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.q.device)
             _check(lib().fp_reset_status(_ptr(self._ws), _stream_handle()), "fp_reset_status")
         return self._ws
+
+    def reset_status(self):
+        _check(lib().fp_reset_status(_ptr(self.workspace()), _stream_handle()), "fp_reset_status")
+
+    def check_wait_timeout(self, limit_ns: int):
+        """fp_check_wait_timeout on this layer's workspace."""
+        _check(lib().fp_check_wait_timeout(_ptr(self.workspace()), int(limit_ns), _stream_handle()),
+               "fp_check_wait_timeout")
 
     def device_status(self) -> int:
         v = c_int(0)

@@ -310,6 +310,14 @@ fp_status fp_device_status(const void *ws, void *stream, int *device_status);
  * records FP_ERR_TIMEOUT and the kernel returns instead of hanging. */
 void fp_set_wait_limit_ns(unsigned long long ns);
 
+/* Failure-path check of the bounded waits, with no GPU fault: launches one
+ * thread that waits, through the kernels' own bounded wait, on an mbarrier
+ * that nothing arrives on, for limit_ns nanoseconds (1 .. 1e10).  The wait
+ * runs out, FP_ERR_TIMEOUT lands in the status word of ws (first error
+ * wins), and the context stays usable: reset the status and carry on.
+ * Returns FP_ERR_INVALID for a null ws or a limit out of range. */
+fp_status fp_check_wait_timeout(void *ws, unsigned long long limit_ns, void *stream);
+
 /* Static description of an fp_status value. */
 const char *fp_status_string(fp_status s);
 

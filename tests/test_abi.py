@@ -116,6 +116,14 @@ def test_odd_group_and_fp8_attention_are_reported_unsupported(fp):
     assert L.fp_dense_attn(ctypes.byref(pr), ctypes.byref(prm), d, None, d, 1 << 30, None) == fp.FP_ERR_UNSUPPORTED
 
 
+def test_wait_timeout_check_refuses_bad_arguments_on_the_host(fp):
+    L = fp.lib()
+    d = ctypes.c_void_p(4096)
+    assert L.fp_check_wait_timeout(None, 1000, None) == fp.FP_ERR_INVALID
+    assert L.fp_check_wait_timeout(d, 0, None) == fp.FP_ERR_INVALID
+    assert L.fp_check_wait_timeout(d, 10_000_000_001, None) == fp.FP_ERR_INVALID
+
+
 def test_status_strings(fp):
     for s in range(7):
         assert fp.status_string(s) and fp.status_string(s) != "unknown status"

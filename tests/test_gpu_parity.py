@@ -325,6 +325,33 @@ def test_index_entry_out_of_range_sets_status():
     assert layer.device_status() == fprefill.FP_ERR_DEVICE_BOUNDS
 
 
+def test_a_wait_that_runs_out_reports_timeout_and_the_context_stays_usable():
+    """The bounded wait the kernels use gives up on a barrier that nothing
+    completes: FP_ERR_TIMEOUT lands in the status word, no fault, and the
+    same workspace then serves a normal attention call with the same result
+    as before."""
+    import torch
+    from block_sparse_long_fp_gb300 import fprefill
+    spec = synth.Spec("timeout", [(700, 0), (300, 256)], 8, 2, page_size=64, layout="shuffled", n_needles=1,
+                      logit_scale=6.0, config_id=75)
+    case = synth.make_case(spec)
+    layer = fprefill.layer_from_case(case)
+    k_mean, v_mean, score = layer.discover()
+    row_ptr, col_idx, nnz = layer.select(score)
+    out, lse = layer.sparse_attn(row_ptr, col_idx, k_mean, v_mean)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    ref_out, ref_lse = out.clone(), lse.clone()
+    layer.check_wait_timeout(2_000_000)               # 2 ms on a barrier nothing arrives on
+    torch.cuda.synchronize()
+    assert layer.device_status() == fprefill.FP_ERR_TIMEOUT
+    layer.reset_status()
+    out2, lse2 = layer.sparse_attn(row_ptr, col_idx, k_mean, v_mean)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    assert torch.equal(out2, ref_out) and torch.equal(lse2, ref_lse)
+
+
 @pytest.mark.slow
 def test_llama8b_32k_sampled():
     """Workload 2 (32K, 32/8 heads, shuffled 64-token pages): every pooled
