@@ -307,13 +307,15 @@ def run_ours(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    spec = synth.config_spec(args.workload)
+    fp8 = args.dtype == "e4m3"
+    spec = synth.config_spec(args.workload, dtype=args.dtype)
     t0 = time.time()
     case = synth.make_case(spec)
     gen_s = time.time() - t0
     layer = fprefill.layer_from_case(case, device=dev)
     if args.logit_scale != 1.0:
-        layer.q.mul_(args.logit_scale)          # exact for powers of two
+        # exact for powers of two; e4m3 codes carry the scale in the per-head query scales
+        (layer.q_scale if fp8 else layer.q).mul_(args.logit_scale)
     stream = torch.cuda.current_stream()
     flop = dense_equiv_flop(spec)
     layer_splits = layer.kv_splits          # 1: no split-KV merge launch
@@ -338,7 +340,7 @@ def run_ours(args, rank, world):
     clocks = clk.summary()
 
     # --- per-stage breakdown, the attention kernel alone, the dense path ---
-    m = measure_layer(layer, spec, min(args.steps, 5), 1, args.dense_steps, stream)
+    m = measure_layer(layer, spec, min(args.steps, 5), 1, args.dense_steps, stream, fp8=fp8)
     ms_disc, ms_sel, ms_attn, ms_dense = m["ms_disc"], m["ms_sel"], m["ms_attn"], m["ms_dense"]
 
     # --- end to end through the C ABI with host buffers ---
@@ -348,7 +350,7 @@ def run_ours(args, rank, world):
 
     # --- variants in the same line: the sparse regime and FP8-e4m3 ---
     variants = {}
-    if args.variants and rank == 0:
+    if args.variants and rank == 0 and not fp8:
         if args.logit_scale == 1.0:
             layer.q.mul_(16.0)                  # exact: a power of two
             variants["bf16_logit_scale_16"] = summary(
@@ -373,13 +375,14 @@ def run_ours(args, rank, world):
     peaks, peak_kind = load_peaks()
     attn_flop = stats["kept_flop"] + stats["corr_flop"]
     achieved = attn_flop / (ms_attn * 1e-3) / 1e12
-    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    # e4m3 runs kind::f8f6f4 MMAs: twice the measured bf16 rate (the nominal fp8 / bf16 ratio)
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * (2.0 if fp8 else 1.0)
     value = whole_job_value(flop, ms, world)
-    q_bytes = spec.total_q * spec.h_q * spec.d * 2
+    q_bytes = spec.total_q * spec.h_q * spec.d * (1 if fp8 else 2)
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
         "data": "synthetic (seeded block-coherent Q/K with sink and needles, V ~ N(0,1))",
         "config": {"workload": spec.name, "batch": spec.batch, "seq_len": spec.total_q,
                    "h_q": spec.h_q, "h_kv": spec.h_kv, "d": spec.d, "page_size": spec.page_size,
@@ -396,7 +399,7 @@ def run_ours(args, rank, world):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic(spec, args.logit_scale),
                      "kernel": "attn_kernel (fp_sparse_attn)",
-                     "peak_source": f"{peak_kind} bf16 sustained (MEASURED_PEAKS.json)"},
+                     "peak_source": f"{peak_kind} bf16 sustained (MEASURED_PEAKS.json)" + (" x 2 for e4m3" if fp8 else "")},
         "gpu_launches": (9 + (1 if layer_splits > 1 else 0)) * args.steps,
         "device_status": status,
         "clocks": clocks,
@@ -522,6 +525,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=3)
     ap.add_argument("--logit-scale", type=float, default=1.0)
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3"],
+                    help="arithmetic of the main workload (the variants run only with bf16)")
     ap.add_argument("--dense-steps", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
