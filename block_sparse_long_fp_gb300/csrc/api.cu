@@ -82,6 +82,8 @@ fp_status check_kv(const fp_problem *p, const BatchDesc &bd) {
     for (int r = 0; r < bd.batch; ++r)
         if ((bd.req[r].lk + ps - 1) / ps > p->max_pages_per_seq) return FP_ERR_INVALID;
     if (p->dtype == FP_E4M3 && (!p->k_scale || !p->v_scale)) return FP_ERR_INVALID;
+    if (p->v_layout != FP_V_TOKEN_MAJOR && p->v_layout != FP_V_DIM_MAJOR) return FP_ERR_INVALID;
+    if (p->v_layout == FP_V_DIM_MAJOR && ps % (p->dtype == FP_E4M3 ? 128 : 64) != 0) return FP_ERR_UNSUPPORTED;
     return FP_OK;
 }
 
@@ -215,7 +217,8 @@ fp_status fp_discover(const fp_problem *p, const fp_params *prm, float *k_mean, 
     const bool fp8 = p->dtype == FP_E4M3;
     if (bd.total_kb > 0 &&
         launch_pool(bd, fp8, p->k_cache, p->v_cache, p->page_size, p->num_pages, p->block_table,
-                    p->max_pages_per_seq, p->k_scale, p->v_scale, k_mean, v_mean, status_ptr(ws), st) != cudaSuccess)
+                    p->max_pages_per_seq, p->k_scale, p->v_scale, k_mean, v_mean, status_ptr(ws), st,
+                    p->v_layout == FP_V_DIM_MAJOR) != cudaSuccess)
         return FP_ERR_CUDA;
     if (bd.total_rows > 0) {
         cudaError_t e;
@@ -291,7 +294,8 @@ fp_status fp_discover_select(const fp_problem *p, const fp_params *prm, float *k
     const int local_blocks = (prm->local_tokens + kBlock - 1) / kBlock;
     if (bd.total_kb > 0 &&
         launch_pool(bd, fp8, p->k_cache, p->v_cache, p->page_size, p->num_pages, p->block_table,
-                    p->max_pages_per_seq, p->k_scale, p->v_scale, k_mean, v_mean, status_ptr(ws), st) != cudaSuccess)
+                    p->max_pages_per_seq, p->k_scale, p->v_scale, k_mean, v_mean, status_ptr(ws), st,
+                    p->v_layout == FP_V_DIM_MAJOR) != cudaSuccess)
         return FP_ERR_CUDA;
     if (bd.total_rows == 0) {
         return cudaMemsetAsync(row_ptr, 0, sizeof(int), st) == cudaSuccess &&
@@ -380,6 +384,7 @@ static fp_status run_attn(const fp_problem *p, const fp_params *prm, const int *
     L.part_lse = n_split > 1 ? reinterpret_cast<float *>(w + off) : nullptr;
     L.wait_ns = g_wait_ns;
     L.fp8 = p->dtype == FP_E4M3;
+    L.v_dim_major = p->v_layout == FP_V_DIM_MAJOR;
     L.q_scale = p->q_scale;
     L.k_scale = p->k_scale;
     L.v_scale = p->v_scale;

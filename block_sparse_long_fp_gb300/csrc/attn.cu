@@ -159,7 +159,9 @@ __device__ __forceinline__ Unit decode_unit(const BatchDesc &bd, const AttnArgs 
 // kLse (e4m3 only): also keep the sum of the unrounded weights, for an LSE
 // that counts the weights e4m3 flushes (wanted when the caller asks for the
 // LSE or rows are split; it costs ~10% of the e4m3 kernel)
-template <bool kFp8, bool kLse>
+// kVdm: the value cache is dim-major ([num_pages, h_kv, d, page_size]): a kept
+// block's V tile arrives as d rows of keys and is a K-major operand of PV
+template <bool kFp8, bool kLse, bool kVdm>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtensorMap tmQ,
             const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -417,7 +419,17 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                                 // e4m3 mean K tiles carry a second (lo) term in the slot's upper half
                                 const bool two = kFp8 && !kept && op == 0;
                                 mbar_expect_tx(full, two ? 2 * kT : kT);
-                                if (kept) {
+                                if (kept && kVdm && op == 1) {
+                                    // d rows of 128 / esz keys per box (K-major): bf16 as two
+                                    // 64-key halves, e4m3 as one box; a pool row z is page
+                                    // z / page_size, key z % page_size (past the pool: zeros)
+#pragma unroll
+                                    for (int hf = 0; hf < kNH; ++hf) {
+                                        const int z = zs[(hf * 64) / rpb] + (hf * 64) % rpb;
+                                        tma_load_3d(dst + hf * kHalfBytes, &tmV, full, z % a.page_size, U.h * kHeadDim,
+                                                    z / a.page_size);
+                                    }
+                                } else if (kept) {
                                     const CUtensorMap *tm = op == 0 ? &tmK : &tmV;
 #pragma unroll
                                     for (int sub = 0; sub < 8; ++sub)
@@ -465,6 +477,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             const uint64_t qdesc = smem_desc_sw128(sbase + kSmemQ, 16, 1024);
             const uint64_t kdesc = smem_desc_sw128(sbase + kSmemK, 16, 1024);
             const uint64_t vdesc = smem_desc_sw128(sbase + kSmemV, kFp8 ? 16 : kHalfBytes, 1024);
+            const uint64_t kvdesc = smem_desc_sw128(sbase + kSmemV, 16, 1024);   // K-major V tiles (kVdm)
             // two: an e4m3 mean tile, whose keys come as hi + lo terms (the lo
             // tile sits in the upper half of the slot)
             auto issue_S = [&](int t, int s, bool two) {
@@ -484,7 +497,20 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     }
                 }
             };
-            auto issue_PV = [&](int t, int s, bool acc) {
+            // kept: a kept block's tile, K-major when the value cache is dim-major
+            // (the same descriptors and steps as the K operand of S); mean tiles
+            // and token-major tiles are MN-major
+            auto issue_PV = [&](int t, int s, bool acc, bool kept) {
+                if (kVdm && kept) {
+                    const uint64_t vd = kvdesc + ((s * kTileBytes) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < kKSteps; ++kk) {
+                        const uint32_t off = (kFp8 ? kk * 32 : (kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                        if constexpr (kFp8) mma_ts_f8(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, vd + off, idS, (acc || kk > 0));
+                        else mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, vd + off, idS, (acc || kk > 0));
+                    }
+                    return;
+                }
                 const uint64_t vd = vdesc + ((s * kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kKSteps; ++kk) {
@@ -523,7 +549,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         break;
                     }
                     tc_fence_after();
-                    issue_PV(0, s, j > 0);
+                    issue_PV(0, s, j > 0, j < first_mean);
                     if (more) {
                         if (!mbar_wait(bar(BAR_KF + s1), ph1, abort_flag, a.status, a.wait_ns)) {
                             good = false;
@@ -540,7 +566,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         break;
                     }
                     tc_fence_after();
-                    issue_PV(1, s, j > 0);
+                    issue_PV(1, s, j > 0, j < first_mean);
                     tc_commit(bar(BAR_VE + s));
                     if (more) {
                         issue_S(1, s1, j + 1 >= first_mean);
@@ -1077,6 +1103,29 @@ static bool make_map(CUtensorMap *m, const void *base, long long n1, long long n
     return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a dim-major value cache [num_pages][h_kv * 128][page_size]:
+// box (128 bytes of keys, the 128 d rows of one head, one page), 128-byte
+// swizzle, zero fill out of bounds (a page index past the pool reads zeros).
+static bool make_map_dm(CUtensorMap *m, const void *base, int h_kv, int page_size, int num_pages, bool fp8) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        fail("cuTensorMapEncodeTiled lookup", 0);
+        return false;
+    }
+    const int esz = fp8 ? 1 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)page_size, (cuuint64_t)h_kv * kHeadDim, (cuuint64_t)num_pages};
+    cuuint64_t strides[2] = {(cuuint64_t)page_size * esz, (cuuint64_t)h_kv * kHeadDim * page_size * esz};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / esz), (cuuint32_t)kHeadDim, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS && debug_on())
+        fprintf(stderr, "[fprefill] dim-major V map (%d,%d,%d): CUresult %d\n", page_size, h_kv * kHeadDim, num_pages,
+                (int)r);
+    return r == CUDA_SUCCESS;
+}
+
 int attn_smem_bytes() { return kSmemAttn; }
 
 // The failure path of the bounded waits, without a fault: one thread waits on
@@ -1113,7 +1162,8 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     if (!make_map(&tmQ, L.q, bd.h_q, total_q, L.q_stride_head, L.q_stride_tok, kBlock, f8)) return fail("Q map", 0);
     if (!make_map(&tmK, L.k_cache, bd.h_kv, tokens, kHeadDim, (long long)bd.h_kv * kHeadDim, rpb, f8))
         return fail("K map", 0);
-    if (!make_map(&tmV, L.v_cache, bd.h_kv, tokens, kHeadDim, (long long)bd.h_kv * kHeadDim, rpb, f8))
+    if (L.v_dim_major ? !make_map_dm(&tmV, L.v_cache, bd.h_kv, L.page_size, L.num_pages, f8)
+                      : !make_map(&tmV, L.v_cache, bd.h_kv, tokens, kHeadDim, (long long)bd.h_kv * kHeadDim, rpb, f8))
         return fail("V map", 0);
     const bool use_means = sparse && L.mean_corr;
     cudaError_t e;
@@ -1166,7 +1216,11 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     a.status = L.status;
     a.wait_ns = L.wait_ns;
     const bool want_lse = L.lse != nullptr || n_split > 1;
-    auto kern = f8 ? (want_lse ? attn_kernel<true, true> : attn_kernel<true, false>) : attn_kernel<false, false>;
+    auto kern = L.v_dim_major
+                    ? (f8 ? (want_lse ? attn_kernel<true, true, true> : attn_kernel<true, false, true>)
+                          : attn_kernel<false, false, true>)
+                    : (f8 ? (want_lse ? attn_kernel<true, true, false> : attn_kernel<true, false, false>)
+                          : attn_kernel<false, false, false>);
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttn)) != cudaSuccess)
         return fail("attention smem attribute", (int)e);
     // persistent: one CTA per SM (the shared memory admits one), never more than units

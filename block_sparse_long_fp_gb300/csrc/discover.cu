@@ -23,7 +23,7 @@ pool_kernel(const __grid_constant__ BatchDesc bd, const uint8_t *__restrict__ k_
             const uint8_t *__restrict__ v_cache, int page_size, int num_pages,
             const int *__restrict__ block_table, int max_pages,
             const float *__restrict__ k_scale, const float *__restrict__ v_scale,
-            float *__restrict__ k_mean, float *__restrict__ v_mean, int *status) {
+            float *__restrict__ k_mean, float *__restrict__ v_mean, int *status, int v_dim_major) {
     constexpr int kEsz = kFp8 ? 1 : 2;
     constexpr int kEpv = 16 / kEsz;  // elements per 16-byte vector
     __shared__ float red[256 * kEpv];
@@ -57,7 +57,28 @@ pool_kernel(const __grid_constant__ BatchDesc bd, const uint8_t *__restrict__ k_
         }
         long long off = ((long long)pg * page_size + t % page_size) * tok_bytes + (long long)vec * 16;
         int4 kv = __ldg(reinterpret_cast<const int4 *>(k_cache + off));
-        int4 vv = __ldg(reinterpret_cast<const int4 *>(v_cache + off));
+        int4 vv;
+        if (!v_dim_major) {
+            vv = __ldg(reinterpret_cast<const int4 *>(v_cache + off));
+        } else {
+            // [num_pages, h_kv, d, page_size]: this vector's kEpv values of token t
+            // sit page_size elements apart
+            const long long e0 = ((long long)pg * bd.h_kv * kHeadDim + (long long)vec * kEpv) * page_size + t % page_size;
+            uint32_t w4[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t w = 0;
+#pragma unroll
+                for (int b = 0; b < 4 / kEsz; ++b) {
+                    const long long e = e0 + (long long)(q * (4 / kEsz) + b) * page_size;
+                    const uint32_t x = kFp8 ? (uint32_t)__ldg(v_cache + e)
+                                            : (uint32_t)__ldg(reinterpret_cast<const uint16_t *>(v_cache) + e);
+                    w |= x << (8 * kEsz * b);
+                }
+                w4[q] = w;
+            }
+            vv = make_int4((int)w4[0], (int)w4[1], (int)w4[2], (int)w4[3]);
+        }
         const uint32_t *kw = reinterpret_cast<const uint32_t *>(&kv);
         const uint32_t *vw = reinterpret_cast<const uint32_t *>(&vv);
         if constexpr (!kFp8) {
@@ -283,18 +304,18 @@ size_t score_smem_bytes(int max_nkb) {
 cudaError_t launch_pool(const BatchDesc &bd, bool fp8, const void *k_cache, const void *v_cache,
                         int page_size, int num_pages, const int *block_table, int max_pages,
                         const float *k_scale, const float *v_scale, float *k_mean, float *v_mean,
-                        int *status, cudaStream_t st) {
+                        int *status, cudaStream_t st, bool v_dim_major) {
     const int epv = fp8 ? 16 : 8;
     const int vpt = bd.h_kv * kHeadDim / epv;
     dim3 grid(bd.total_kb, vpt > 256 ? vpt / 256 : 1);
     if (fp8)
         pool_kernel<true><<<grid, 256, 0, st>>>(bd, (const uint8_t *)k_cache, (const uint8_t *)v_cache,
                                                 page_size, num_pages, block_table, max_pages, k_scale,
-                                                v_scale, k_mean, v_mean, status);
+                                                v_scale, k_mean, v_mean, status, v_dim_major ? 1 : 0);
     else
         pool_kernel<false><<<grid, 256, 0, st>>>(bd, (const uint8_t *)k_cache, (const uint8_t *)v_cache,
                                                  page_size, num_pages, block_table, max_pages, k_scale,
-                                                 v_scale, k_mean, v_mean, status);
+                                                 v_scale, k_mean, v_mean, status, v_dim_major ? 1 : 0);
     return cudaGetLastError();
 }
 

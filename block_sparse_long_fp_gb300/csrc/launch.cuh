@@ -6,7 +6,8 @@
 namespace fp {
 cudaError_t launch_pool(const BatchDesc &bd, bool fp8, const void *k_cache, const void *v_cache, int page_size,
                         int num_pages, const int *block_table, int max_pages, const float *k_scale,
-                        const float *v_scale, float *k_mean, float *v_mean, int *status, cudaStream_t st);
+                        const float *v_scale, float *k_mean, float *v_mean, int *status, cudaStream_t st,
+                        bool v_dim_major = false);
 cudaError_t launch_score(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
                          long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
                          float *score, cudaStream_t st);
@@ -58,6 +59,7 @@ struct AttnLaunch {
     int n_split;                      // split-KV parts per row (1: none)
     float *part_o;                    // [n_split, total_q, h_q, d] fp32 when n_split > 1
     float *part_lse;                  // [n_split, h_q, total_q] fp32 when n_split > 1
+    bool v_dim_major;                 // value cache [num_pages, h_kv, d, page_size]
 };
 int launch_attn(const AttnLaunch &L, cudaStream_t st);
 // rows of the bf16 block-mean copies: at least one full 128-row TMA box

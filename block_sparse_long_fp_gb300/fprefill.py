@@ -21,6 +21,7 @@ FP_BF16, FP_E4M3 = 0, 1
 FP_MAX_BATCH = 128
 FP_SELECT_THRESHOLD, FP_SELECT_TOPK, FP_SELECT_TOPP = 0, 1, 2
 FP_SCORE_PACKED, FP_SCORE_HEAD_UNION = 0, 1
+FP_V_TOKEN_MAJOR, FP_V_DIM_MAJOR = 0, 1
 
 
 class FpParams(Structure):
@@ -36,7 +37,7 @@ class FpProblem(Structure):
                 ("q", c_void_p), ("q_stride_tok", c_longlong), ("q_stride_head", c_longlong),
                 ("k_cache", c_void_p), ("v_cache", c_void_p), ("page_size", c_int),
                 ("num_pages", c_int), ("block_table", c_void_p), ("max_pages_per_seq", c_int),
-                ("q_scale", c_void_p), ("k_scale", c_void_p), ("v_scale", c_void_p)]
+                ("q_scale", c_void_p), ("k_scale", c_void_p), ("v_scale", c_void_p), ("v_layout", c_int)]
 
 
 class FprefillError(RuntimeError):
@@ -122,14 +123,16 @@ class Layer:
     """One attention layer's operands: device tensors (q, paged k/v caches,
     block table, FP8 scales) plus the host varlen descriptors.
 
-    q: [total_q, h_q, 128] bf16 (or uint8 e4m3 codes); k_cache / v_cache:
-    [num_pages, page_size, h_kv, 128]; block_table: int32 [batch, max_pages].
+    q: [total_q, h_q, 128] bf16 (or uint8 e4m3 codes); k_cache:
+    [num_pages, page_size, h_kv, 128]; v_cache: the same, or
+    [num_pages, h_kv, 128, page_size] with v_layout = FP_V_DIM_MAJOR;
+    block_table: int32 [batch, max_pages].
     cu_seqlens_q / seqlens_k / q_start_pos: host int sequences.
     """
 
     def __init__(self, q, k_cache, v_cache, block_table, cu_seqlens_q, seqlens_k, q_start_pos,
                  h_q: int, h_kv: int, dtype: str = "bf16", q_scale=None, k_scale=None, v_scale=None,
-                 params: FpParams | None = None):
+                 params: FpParams | None = None, v_layout: int = 0):
         self.q, self.k_cache, self.v_cache, self.block_table = q, k_cache, v_cache, block_table
         self.q_scale, self.k_scale, self.v_scale = q_scale, k_scale, v_scale
         self.cu = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
@@ -153,6 +156,7 @@ class Layer:
         pr.block_table = _ptr(block_table)
         pr.max_pages_per_seq = int(block_table.shape[1])
         pr.q_scale, pr.k_scale, pr.v_scale = _ptr(q_scale), _ptr(k_scale), _ptr(v_scale)
+        pr.v_layout = int(v_layout)
         self.problem = pr
         L = lib()
         pp, pm = ctypes.byref(pr), ctypes.byref(self.params)
@@ -284,22 +288,25 @@ class Layer:
         return out, lse, (row_ptr, col_idx, nnz)
 
 
-def layer_from_case(case, device="cuda", params: FpParams | None = None):
-    """Upload a synthetic case (block_sparse_long_fp_gb300.synth.Case) and wrap it."""
+def layer_from_case(case, device="cuda", params: FpParams | None = None, v_layout: int = 0):
+    """Upload a synthetic case (block_sparse_long_fp_gb300.synth.Case) and wrap it.
+    v_layout = FP_V_DIM_MAJOR uploads the value cache as [num_pages, h_kv, 128,
+    page_size] (the same values, keys contiguous)."""
     import torch
     spec = case.spec
+    v_host = case.v_cache if v_layout == FP_V_TOKEN_MAJOR else np.ascontiguousarray(case.v_cache.transpose(0, 2, 3, 1))
     if spec.dtype == "bf16":
         q = torch.from_numpy(case.q).view(torch.bfloat16).to(device)
         k = torch.from_numpy(case.k_cache).view(torch.bfloat16).to(device)
-        v = torch.from_numpy(case.v_cache).view(torch.bfloat16).to(device)
+        v = torch.from_numpy(v_host).view(torch.bfloat16).to(device)
         qs = ks = vs = None
     else:
         q = torch.from_numpy(case.q).to(device)
         k = torch.from_numpy(case.k_cache).to(device)
-        v = torch.from_numpy(case.v_cache).to(device)
+        v = torch.from_numpy(v_host).to(device)
         qs = torch.from_numpy(case.q_scale).to(device)
         ks = torch.from_numpy(case.k_scale).to(device)
         vs = torch.from_numpy(case.v_scale).to(device)
     bt = torch.from_numpy(case.block_table).to(device)
     return Layer(q, k, v, bt, case.cu_seqlens_q, case.seqlens_k, case.q_start_pos, spec.h_q, spec.h_kv,
-                 dtype=spec.dtype, q_scale=qs, k_scale=ks, v_scale=vs, params=params)
+                 dtype=spec.dtype, q_scale=qs, k_scale=ks, v_scale=vs, params=params, v_layout=v_layout)

@@ -149,7 +149,18 @@ typedef struct {
     const float *q_scale;         /* [h_q]   FP_E4M3 only (may be NULL for FP_BF16) */
     const float *k_scale;         /* [h_kv]  FP_E4M3 only */
     const float *v_scale;         /* [h_kv]  FP_E4M3 only */
+    int v_layout;                 /* fp_v_layout of v_cache (0: token-major, like k_cache) */
 } fp_problem;
+
+/* Layout of the value cache [V2 popular article, FP8 passage: a value cache
+ * stored by rows or by columns].  TOKEN_MAJOR: [num_pages, page_size, h_kv, d],
+ * the layout of k_cache.  DIM_MAJOR: [num_pages, h_kv, d, page_size], each
+ * (page, head, d) holding the page's tokens contiguously; page_size must be a
+ * multiple of 64 for FP_BF16 and of 128 for FP_E4M3 (FP_ERR_UNSUPPORTED
+ * otherwise).  The result is the same either way (up to the summation order
+ * of the PV product); the attention takes DIM_MAJOR tiles as K-major operands
+ * and TOKEN_MAJOR ones as MN-major operands, so neither is transposed on chip. */
+typedef enum { FP_V_TOKEN_MAJOR = 0, FP_V_DIM_MAJOR = 1 } fp_v_layout;
 
 /* Defaults of the pages: B=128, sink 256, local 512, alpha 0.1, 1/sqrt(d),
  * mean correction on [V2 paper reading, section 4 configuration]; kv_splits 0

@@ -13,11 +13,12 @@ FP8_LSE_ABS = 2e-2
 SCORE_ABS = 2e-6          # scores lie in (0, 1]; fp32 evaluation error is ~1e-7
 
 
-def gpu_stage_outputs(case, alpha=0.1, mean_corr=True, dense=False, kv_splits=0, select=None, attention=True):
+def gpu_stage_outputs(case, alpha=0.1, mean_corr=True, dense=False, kv_splits=0, select=None, attention=True,
+                      v_layout=0):
     import torch
     from block_sparse_long_fp_gb300 import fprefill
     prm = fprefill.default_params(alpha=alpha, mean_correction=int(mean_corr), kv_splits=kv_splits, **(select or {}))
-    layer = fprefill.layer_from_case(case, params=prm)
+    layer = fprefill.layer_from_case(case, params=prm, v_layout=v_layout)
     k_mean, v_mean, score = layer.discover()
     row_ptr, col_idx, nnz = layer.select(score)
     if not attention:

@@ -116,6 +116,23 @@ def test_odd_group_and_fp8_attention_are_reported_unsupported(fp):
     assert L.fp_dense_attn(ctypes.byref(pr), ctypes.byref(prm), d, None, d, 1 << 30, None) == fp.FP_ERR_UNSUPPORTED
 
 
+def test_value_cache_layout_is_checked_on_the_host(fp):
+    prm = fp.default_params()
+    L = fp.lib()
+    d = ctypes.c_void_p(4096)
+    pr, keep = problem(fp, [(300, 0)], page=64)
+    pr.v_layout = 2
+    assert L.fp_dense_attn(ctypes.byref(pr), ctypes.byref(prm), d, None, d, 1 << 30, None) == fp.FP_ERR_INVALID
+    pr, keep = problem(fp, [(300, 0)], page=32)
+    pr.v_layout = fp.FP_V_DIM_MAJOR            # bf16 needs pages of a multiple of 64 tokens
+    assert L.fp_dense_attn(ctypes.byref(pr), ctypes.byref(prm), d, None, d, 1 << 30, None) == fp.FP_ERR_UNSUPPORTED
+    pr, keep = problem(fp, [(300, 0)], page=64)
+    pr.dtype = fp.FP_E4M3                      # e4m3 needs a multiple of 128
+    pr.q_scale = pr.k_scale = pr.v_scale = 4096
+    pr.v_layout = fp.FP_V_DIM_MAJOR
+    assert L.fp_dense_attn(ctypes.byref(pr), ctypes.byref(prm), d, None, d, 1 << 30, None) == fp.FP_ERR_UNSUPPORTED
+
+
 def test_wait_timeout_check_refuses_bad_arguments_on_the_host(fp):
     L = fp.lib()
     d = ctypes.c_void_p(4096)

@@ -22,15 +22,16 @@ def built():
 
 
 def full_parity(spec, alpha=0.1, mean_corr=True, rows_per_request=None, max_abs=None, mean_abs=None,
-                lse_abs=2e-2, select=None):
-    """select: {select_rule, top_k, top_p} for the top-k / top-p ablations."""
+                lse_abs=2e-2, select=None, v_layout=0):
+    """select: {select_rule, top_k, top_p} for the top-k / top-p ablations;
+    v_layout: the value cache's layout on the GPU (the oracle reads the same values)."""
     import oracle
     from parity_util import BF16_MAX_ABS, BF16_MEAN_ABS
     case = synth.make_case(spec)
     sel = select or {}
     ref = oracle.discover_and_select(case, alpha=alpha, rule=sel.get("select_rule", 0), top_k=sel.get("top_k", 0),
                                      top_p=sel.get("top_p", 0.0), head_union=sel.get("score_mode", 0) == 1)
-    g = gpu_stage_outputs(case, alpha=alpha, mean_corr=mean_corr, select=select)
+    g = gpu_stage_outputs(case, alpha=alpha, mean_corr=mean_corr, select=select, v_layout=v_layout)
     assert g["status"] == 0
     check_pool(case, g, ref)
     flips = check_scores_and_index(case, g, ref)
@@ -165,14 +166,14 @@ def test_empty_rows_and_rows_without_their_diagonal_block(mean_corr, kv_splits):
     assert n_void > 0
 
 
-@pytest.mark.parametrize("kv_splits", [0, 4])
-def test_dense_path_equals_causal_softmax(kv_splits):
+@pytest.mark.parametrize("kv_splits,v_layout", [(0, 0), (4, 0), (0, 1)])
+def test_dense_path_equals_causal_softmax(kv_splits, v_layout):
     import oracle
     spec = synth.Spec("dense", [(1000, 0), (384, 256)], 4, 2, page_size=64, layout="shuffled",
                       n_needles=1, config_id=72)
     case = synth.make_case(spec)
     ref = oracle.discover_and_select(case)
-    g = gpu_stage_outputs(case, dense=True, kv_splits=kv_splits)
+    g = gpu_stage_outputs(case, dense=True, kv_splits=kv_splits, v_layout=v_layout)
     assert g["status"] == 0
     oref = oracle_outputs(case, ref, mean_corr=False, dense=True)
     check_outputs(case, g, oref)
@@ -419,6 +420,25 @@ def test_fp8_attention_sharp_varlen(mean_corr):
     from parity_util import FP8_LSE_ABS
     r = full_parity(spec, mean_corr=mean_corr, rows_per_request=2000, max_abs=0.1, mean_abs=6e-3,
                     lse_abs=FP8_LSE_ABS)
+    assert r["density"] < 0.95
+
+
+@pytest.mark.parametrize("dtype,page", [("bf16", 64), ("bf16", 256), ("e4m3", 128), ("e4m3", 256)])
+def test_dim_major_value_cache(dtype, page):
+    """The value cache stored dim-major, [num_pages, h_kv, d, page_size] with
+    each page's keys contiguous (the column-stored values of the V2 popular
+    article's FP8 passage).  Pooling reads it in place; the attention takes a
+    kept block's V tile as a K-major operand (mean tiles keep their own
+    token-major copies).  The whole path against the oracle, which reads the
+    same values token-major, on a ragged varlen batch with a chunk and skipped
+    blocks."""
+    from parity_util import FP8_LSE_ABS
+    spec = synth.Spec("v-dim-major", [(2048, 0), (3000, 0), (256, 512)], 8, 2, page_size=page, layout="shuffled",
+                      dtype=dtype, n_needles=2, logit_scale=6.0, config_id=76)
+    if dtype == "bf16":
+        r = full_parity(spec, v_layout=1, rows_per_request=2000)
+    else:
+        r = full_parity(spec, v_layout=1, rows_per_request=2000, max_abs=0.1, mean_abs=6e-3, lse_abs=FP8_LSE_ABS)
     assert r["density"] < 0.95
 
 
