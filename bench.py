@@ -13,6 +13,14 @@ headline value is dense-equivalent TFLOP/s = 4 * d * H_q * (causal query-key
 pairs) / (ms per layer); ms per layer is reported beside it.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--dtype bf16|e4m3] [--alpha A] [--no-mean-correction] [--logit-scale C]
+
+The same JSON line carries `variants`: the 128K layer with queries x 16 (the
+pages' sparse regime; mean correction on and off, and the top-k / top-p /
+union-of-heads ablations), in e4m3, a chunked-prefill step with split-KV,
+the 32K layer (mean correction on and off), the six-request varlen batch, and
+the 256K density/error sweep over alpha x mean correction x {bf16, e4m3} x
+{as specified, queries x 16} with errors against the float64 oracle.
 
 With --gpus N > 1 (under torchrun) every rank runs an independent replica of
 the layer (the path has no exchange step): weak scaling, value = the work of
@@ -156,6 +164,7 @@ def whole_job_value(flop_per_replica: float, ms: float, world: int) -> float:
 
 
 def cuda_time(fn, steps, stream):
+    """Mean ms of `steps` back-to-back calls (one event pair around them)."""
     import torch
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
@@ -167,24 +176,36 @@ def cuda_time(fn, steps, stream):
     return a.elapsed_time(b) / steps
 
 
+def cuda_median(fn, reps, stream):
+    """Median ms over `reps` calls, each bracketed by its own event pair on
+    the launching stream (the calls still run back to back)."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    ev[-1][1].synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
 def recorded_traffic(spec, logit_scale):
     """DRAM bytes per attention launch of this workload from the committed ncu
-    record, or None when the record is for another workload or the kernel's
-    sources changed since it was taken."""
+    record (profiles/attn_traffic.json), or None when the record is for another
+    workload or the kernel's sources changed since it was taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "attn_kernel_traffic_qwen30b_128k.md")
-    if spec.name != "qwen30b-128k" or spec.dtype != "bf16" or logit_scale != 1.0 or not os.path.exists(path):
+    path = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    if not os.path.exists(path):
         return None
-    rec = {}
-    for line in open(path):
-        if ":" in line and line.split(":")[0] in ("traffic_bytes_per_launch", "kernel_sources_sha256"):
-            k, v = line.split(":", 1)
-            rec[k.strip()] = v.strip()
+    rec = json.load(open(path))
+    if (spec.name != rec.get("workload") or spec.dtype != rec.get("dtype")
+            or logit_scale != rec.get("logit_scale")):
+        return None
     csrc = os.path.join(ROOT, "block_sparse_long_fp_gb300", "csrc")
     src = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("attn.cu", "sm100.cuh", "common.cuh", "launch.cuh"))
     if rec.get("kernel_sources_sha256") != hashlib.sha256(src).hexdigest():
         return None
-    return int(float(rec["traffic_bytes_per_launch"]))
+    return int(rec["traffic_bytes_per_launch"])
 
 
 def load_peaks():
@@ -195,8 +216,21 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def measure_layer(layer, spec, steps, warmup, dense_steps, stream, fp8=False):
-    """Time the whole step and each stage on one uploaded layer."""
+def launches_per_step(layer) -> int:
+    """Kernels one step launches: fp_discover (pool, split of the key means,
+    score), fp_select (the one-pass select kernel), fp_sparse_attn (copy of the
+    block means for the mean tiles when the correction is on, schedule,
+    attention, and the split-KV merge when rows are split)."""
+    mc = 1 if layer.params.mean_correction else 0
+    return 3 + SELECT_LAUNCHES + (mc + 2) + (1 if layer.kv_splits > 1 else 0)
+
+
+SELECT_LAUNCHES = 3
+
+
+def measure_layer(layer, spec, reps, warmup, dense_reps, stream, fp8=False):
+    """Time the whole step and each stage on one uploaded layer (medians of
+    `reps` event-timed calls; the dense path over `dense_reps`)."""
     import torch
     flop = dense_equiv_flop(spec)
     for _ in range(warmup):
@@ -204,37 +238,38 @@ def measure_layer(layer, spec, steps, warmup, dense_steps, stream, fp8=False):
     torch.cuda.synchronize()
     status = layer.device_status()
     stats = index_stats(spec, row_ptr.cpu().numpy())
-    ms = cuda_time(lambda: layer.prefill(), steps, stream)
+    ms = cuda_median(lambda: layer.prefill(), reps, stream)
     k_mean, v_mean, score = layer.discover()
     rp, ci, nz = layer.select(score)
-    reps = max(2, min(steps, 5))
     out_buf = torch.empty((layer.total_q, layer.h_q, 128), dtype=torch.bfloat16, device=layer.q.device)
-    ms_disc = cuda_time(lambda: layer.discover(k_mean, v_mean, score), reps, stream)
-    ms_sel = cuda_time(lambda: layer.select(score, rp, ci, nz), reps, stream)
-    ms_attn = cuda_time(lambda: layer.sparse_attn(rp, ci, k_mean, v_mean, out=out_buf, want_lse=False), reps,
-                        stream)
+    ms_disc = cuda_median(lambda: layer.discover(k_mean, v_mean, score), reps, stream)
+    ms_sel = cuda_median(lambda: layer.select(score, rp, ci, nz), reps, stream)
+    ms_attn = cuda_median(lambda: layer.sparse_attn(rp, ci, k_mean, v_mean, out=out_buf, want_lse=False), reps,
+                          stream)
     # the fused fp_discover_select (no score map) in place of the first two stages
     km2, vm2, rp2, ci2, nz2 = layer.discover_select()
-    ms_dsel = cuda_time(lambda: layer.discover_select(km2, vm2, None, rp2, ci2, nz2), reps, stream)
+    ms_dsel = cuda_median(lambda: layer.discover_select(km2, vm2, None, rp2, ci2, nz2), reps, stream)
     ms_dense = None
-    if dense_steps > 0:
+    if dense_reps > 0:
         layer.dense_attn(out=out_buf, want_lse=False)
-        ms_dense = cuda_time(lambda: layer.dense_attn(out=out_buf, want_lse=False), dense_steps, stream)
+        ms_dense = cuda_median(lambda: layer.dense_attn(out=out_buf, want_lse=False), dense_reps, stream)
     peaks, peak_kind = load_peaks()
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * (2.0 if fp8 else 1.0)
     attn_flop = stats["kept_flop"] + stats["corr_flop"]
     achieved = attn_flop / (ms_attn * 1e-3) / 1e12
     return dict(ms=ms, flop=flop, status=status, stats=stats, ms_disc=ms_disc, ms_sel=ms_sel, ms_attn=ms_attn,
-                ms_dense=ms_dense, ms_dsel=ms_dsel, achieved=achieved, peak=peak, peak_kind=peak_kind)
+                ms_dense=ms_dense, ms_dsel=ms_dsel, achieved=achieved, peak=peak, peak_kind=peak_kind, reps=reps)
 
 
-def summary(m, spec, logit_scale, dtype):
+def summary(m, spec, logit_scale, dtype, alpha=0.1, mean_corr=True):
     return {
-        "dtype": dtype, "logit_scale": logit_scale,
+        "workload": spec.name, "dtype": dtype, "logit_scale": logit_scale, "alpha": alpha,
+        "mean_correction": bool(mean_corr),
         "ms_per_layer": round(m["ms"], 4),
         "dense_equiv_tflops": round(m["flop"] / (m["ms"] * 1e-3) / 1e12, 2),
         "stages_ms": {"discover": round(m["ms_disc"], 4), "select": round(m["ms_sel"], 4),
                       "sparse_attn": round(m["ms_attn"], 4), "discover_select_fused": round(m["ms_dsel"], 4)},
+        "timing": f"medians of {m['reps']} event-timed calls",
         "density": round(m["stats"]["density"], 5),
         "attn_tflops": round(m["achieved"], 2), "attn_peak_tflops": m["peak"],
         "attn_frac": round(m["achieved"] / m["peak"], 4),
@@ -266,10 +301,10 @@ def selection_ablation(layer, spec, stream):
         entry = {}
         if mode != fprefill.FP_SCORE_PACKED:
             k_mean, v_mean, score = layer.discover()
-            entry["discover_ms"] = round(cuda_time(lambda: layer.discover(k_mean, v_mean, score), 3, stream), 4)
+            entry["discover_ms"] = round(cuda_median(lambda: layer.discover(k_mean, v_mean, score), 5, stream), 4)
         rp, ci, nnz = layer.select(score)
         o, _ = layer.sparse_attn(rp, ci, k_mean, v_mean, want_lse=False)
-        ms = cuda_time(lambda: layer.sparse_attn(rp, ci, k_mean, v_mean, out=o, want_lse=False), 3, stream)
+        ms = cuda_median(lambda: layer.sparse_attn(rp, ci, k_mean, v_mean, out=o, want_lse=False), 5, stream)
         stats = index_stats(spec, rp.cpu().numpy())
         err = float(torch.linalg.vector_norm(o[rows].float() - ref) / torch.linalg.vector_norm(ref))
         entry.update({"density": round(stats["density"], 5), "attn_ms": round(ms, 4),
@@ -279,7 +314,7 @@ def selection_ablation(layer, spec, stream):
     return out
 
 
-def chunk_variant(dev, stream, steps, dense_steps):
+def chunk_variant(dev, stream, reps, dense_reps):
     """A chunked-prefill step at long context: 512 queries at position 130560
     (32/4 heads, the 128K layer's shape).  It has 64 work units for 152 SMs, so
     the attention splits each row's key list (split-KV) and merges the parts by
@@ -291,13 +326,162 @@ def chunk_variant(dev, stream, steps, dense_steps):
     out = {"workload": spec.name}
     for name, ks in (("auto_split", 0), ("no_split", 1)):
         layer = fprefill.layer_from_case(case, device=dev, params=fprefill.default_params(kv_splits=ks))
-        res = summary(measure_layer(layer, spec, steps, 2, dense_steps, stream), spec, 1.0, "bf16")
+        res = summary(measure_layer(layer, spec, reps, 2, dense_reps, stream), spec, 1.0, "bf16")
         res["kv_splits"] = layer.kv_splits
         out[name] = res
         del layer
     a, n = out["auto_split"]["stages_ms"]["sparse_attn"], out["no_split"]["stages_ms"]["sparse_attn"]
     out["attn_speedup_from_split"] = round(n / a, 3)
     return out
+
+
+def scale_queries(layer, c: float):
+    """Multiply every query by c (a power of two, so exactly): bf16 queries in
+    place, e4m3 ones through their per-head scales."""
+    (layer.q_scale if layer.problem.dtype == 1 else layer.q).mul_(c)
+
+
+def workload_variants(n, dev, stream, reps, dense_reps, mc_both=False):
+    """Workload n as specified and with queries x 16 (the pages' sparse
+    regime), bf16; with mc_both, each also with the mean correction off."""
+    import torch
+    from block_sparse_long_fp_gb300 import fprefill, synth
+    spec = synth.config_spec(n)
+    case = synth.make_case(spec)
+    layer = fprefill.layer_from_case(case, device=dev)
+    out = {"workload": spec.name}
+    for c in (1.0, 16.0):
+        if c != 1.0:
+            scale_queries(layer, c)
+        for mc in ((1, 0) if mc_both else (1,)):
+            layer.params.mean_correction = mc
+            key = ("as_specified" if c == 1.0 else f"logit_scale_{int(c)}") + ("" if mc else "_mc_off")
+            out[key] = summary(measure_layer(layer, spec, reps, 2, dense_reps if mc else 0, stream), spec, c,
+                               "bf16", mean_corr=mc)
+        layer.params.mean_correction = 1
+    if mc_both:
+        for k in ("as_specified", "logit_scale_16"):
+            on, off = out[k]["stages_ms"]["sparse_attn"], out[k + "_mc_off"]["stages_ms"]["sparse_attn"]
+            out[k]["mean_correction_overhead_ms"] = round(on - off, 4)
+    del layer
+    torch.cuda.empty_cache()
+    return out
+
+
+SWEEP_ALPHAS = (0.2, 0.1, 0.05, 0.025, 0.0125)
+
+
+def density_error_sweep(dev, stream, dtype, reps, oracle_rows=2, oracle_queries=8, seed=0):
+    """Workload 5 (256K, 32/4 heads): kept density, ms per layer and output
+    error for alpha in SWEEP_ALPHAS x mean correction on/off, with queries as
+    specified and x 16.  Errors are taken on sampled query rows of every kv
+    head (4 of 4): O against the float64 oracle on the oracle's own selection
+    (max-abs, mean-abs) and against float64 dense attention (the method's
+    approximation error: max-abs and relative Frobenius).  The
+    mean-correction overhead is attention(on) - attention(off)."""
+    import torch
+    import oracle
+    from block_sparse_long_fp_gb300 import fprefill, synth
+    oracle.build()
+    spec = synth.config_spec(5, dtype=dtype)
+    case = synth.make_case(spec)
+    layer = fprefill.layer_from_case(case, device=dev)
+    lq, start = spec.requests[0]
+    hkv, g, B = spec.h_kv, spec.h_q // spec.h_kv, 128
+    scale = 1 / math.sqrt(spec.d)
+    nqb = -(-lq // B)
+    rng = np.random.default_rng(seed)
+    k, v = oracle.request_kv(case, 0)
+    kbar, vbar = oracle.pool(k, B), oracle.pool(v, B)
+    nkb = kbar.shape[0]
+    blocks = sorted({nqb - 1, *[int(x) for x in rng.integers(8, nqb - 1, oracle_rows - 1)]})
+    sample = []                                # (i, h, query indices in the block, query heads)
+    for h in range(hkv):
+        for i in blocks:
+            n = min(lq, (i + 1) * B) - i * B
+            qi = rng.integers(0, n, oracle_queries)
+            qi[0] = n - 1
+            sample.append((i, h, qi, h * g + rng.integers(0, g, oracle_queries)))
+    offs = layer.score_offsets()
+    out_buf = torch.empty((layer.total_q, layer.h_q, 128), dtype=torch.bfloat16, device=dev)
+    res = {"workload": spec.name, "dtype": dtype, "alphas": list(SWEEP_ALPHAS),
+           "oracle_sample": f"{len(sample)} score rows ({len(blocks)} query blocks x {hkv} kv heads), "
+                            f"{oracle_queries} queries each", "timing": f"medians of {reps} event-timed calls",
+           "points": []}
+    t_oracle = 0.0
+    for c in (1.0, 16.0):
+        if c != 1.0:
+            scale_queries(layer, c)
+        t0 = time.perf_counter()
+        qblk = {}
+        for i in blocks:
+            q0, q1 = i * B, min(lq, (i + 1) * B)
+            qblk[i] = oracle.decode(case.q[q0:q1], dtype) * (case.q_scale.astype(np.float64) * c)[None, :, None]
+        s_ref = {(i, h): oracle.score_rows(qblk[i], start + i * B, hkv, B, scale, kbar, [h])[0]
+                 for i, h, _, _ in sample}
+        dense_ref = {(i, h): oracle.attn_rows(qblk[i], start + i * B, k, v, kbar, vbar, B, scale, None, False,
+                                              qi, qh)[0] for i, h, qi, qh in sample}
+        t_oracle += time.perf_counter() - t0
+        layer.params.mean_correction = 1
+        k_mean, v_mean, score = layer.discover()
+        ms_disc = cuda_median(lambda: layer.discover(k_mean, v_mean, score), reps, stream)
+        for alpha in SWEEP_ALPHAS:
+            layer.params.alpha = alpha
+            rp, ci, nz = layer.select(score)
+            ms_sel = cuda_median(lambda: layer.select(score, rp, ci, nz), reps, stream)
+            rp_h, ci_h = rp.cpu().numpy(), ci.cpu().numpy()
+            stats = index_stats(spec, rp_h)
+            # the GPU's index on the sampled rows against the oracle's selection
+            flips = 0
+            keeps = {}
+            for i, h, _, _ in sample:
+                I = start // B + i
+                keep_ref, flag = oracle.select_row(s_ref[(i, h)], I, alpha, B, 256, 512)
+                row = i * hkv + h
+                kept = np.zeros(I + 1, bool)
+                kept[ci_h[rp_h[row]:rp_h[row + 1]]] = True
+                flips += int(np.count_nonzero((kept != keep_ref) & ~flag))
+                keeps[(i, h)] = keep_ref
+            for mc in (1, 0):
+                layer.params.mean_correction = mc
+                ms_attn = cuda_median(lambda: layer.sparse_attn(rp, ci, k_mean, v_mean, out=out_buf,
+                                                                want_lse=False), reps, stream)
+                e_or, e_de, n2, d2 = [], [], 0.0, 0.0
+                t0 = time.perf_counter()
+                for i, h, qi, qh in sample:
+                    keep = np.zeros((1, hkv, nkb), np.uint8)
+                    keep[0, h, :start // B + i + 1] = keeps[(i, h)]
+                    o_ref, _ = oracle.attn_rows(qblk[i], start + i * B, k, v, kbar, vbar, B, scale, keep, bool(mc),
+                                                qi, qh)
+                    tok = torch.as_tensor(i * B + qi, device=dev)
+                    got = out_buf[tok, torch.as_tensor(qh, device=dev)].float().cpu().numpy()
+                    e_or.append(np.abs(got - o_ref).ravel())
+                    dr = dense_ref[(i, h)]
+                    e_de.append(np.abs(got - dr).ravel())
+                    n2 += float(((got - dr) ** 2).sum())
+                    d2 += float((dr ** 2).sum())
+                t_oracle += time.perf_counter() - t0
+                e_or, e_de = np.concatenate(e_or), np.concatenate(e_de)
+                res["points"].append({
+                    "logit_scale": c, "alpha": alpha, "mean_correction": bool(mc),
+                    "density": round(stats["density"], 5),
+                    "ms_per_layer": round(ms_disc + ms_sel + ms_attn, 4),
+                    "stages_ms": {"discover": round(ms_disc, 4), "select": round(ms_sel, 4),
+                                  "sparse_attn": round(ms_attn, 4)},
+                    "err_vs_oracle": {"max_abs": round(float(e_or.max()), 5), "mean_abs": round(float(e_or.mean()), 6)},
+                    "err_vs_dense": {"max_abs": round(float(e_de.max()), 5),
+                                     "rel_fro": round(math.sqrt(n2 / max(d2, 1e-300)), 5)},
+                    "index_flips_outside_band": flips,
+                })
+            on, off = res["points"][-2], res["points"][-1]
+            on["mean_correction_overhead_ms"] = round(on["stages_ms"]["sparse_attn"] - off["stages_ms"]["sparse_attn"], 4)
+        layer.params.alpha = 0.1
+        layer.params.mean_correction = 1
+    res["oracle_seconds"] = round(t_oracle, 1)
+    res["device_status"] = layer.device_status()
+    del layer, case
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_ours(args, rank, world):
@@ -312,13 +496,12 @@ def run_ours(args, rank, world):
     t0 = time.time()
     case = synth.make_case(spec)
     gen_s = time.time() - t0
-    layer = fprefill.layer_from_case(case, device=dev)
+    prm = fprefill.default_params(alpha=args.alpha, mean_correction=int(args.mean_correction))
+    layer = fprefill.layer_from_case(case, device=dev, params=prm)
     if args.logit_scale != 1.0:
-        # exact for powers of two; e4m3 codes carry the scale in the per-head query scales
-        (layer.q_scale if fp8 else layer.q).mul_(args.logit_scale)
+        scale_queries(layer, args.logit_scale)      # exact for powers of two
     stream = torch.cuda.current_stream()
     flop = dense_equiv_flop(spec)
-    layer_splits = layer.kv_splits          # 1: no split-KV merge launch
 
     # --- warm-up and one index for the statistics ---
     for _ in range(args.warmup):
@@ -339,38 +522,54 @@ def run_ours(args, rank, world):
     ms = max_over_ranks(ms, world, dev)
     clocks = clk.summary()
 
-    # --- per-stage breakdown, the attention kernel alone, the dense path ---
-    m = measure_layer(layer, spec, min(args.steps, 5), 1, args.dense_steps, stream, fp8=fp8)
+    # --- per-stage breakdown (medians over >= 20 calls), the dense path ---
+    m = measure_layer(layer, spec, max(20, args.steps), 1, args.dense_steps, stream, fp8=fp8)
     ms_disc, ms_sel, ms_attn, ms_dense = m["ms_disc"], m["ms_sel"], m["ms_attn"], m["ms_dense"]
+    launches = launches_per_step(layer)
 
     # --- end to end through the C ABI with host buffers ---
     e2e = None
     if args.e2e_steps > 0:
         e2e = run_e2e(layer, args.e2e_steps, flop)
 
-    # --- variants in the same line: the sparse regime and FP8-e4m3 ---
+    # --- variants in the same line: the sparse regime, FP8-e4m3, the other workloads, the sweep ---
     variants = {}
-    if args.variants and rank == 0 and not fp8:
-        if args.logit_scale == 1.0:
-            layer.q.mul_(16.0)                  # exact: a power of two
+    vreps = 10
+    if args.variants and rank == 0 and not fp8 and args.workload == 3:
+        if args.logit_scale == 1.0 and args.mean_correction and args.alpha == 0.1:
+            scale_queries(layer, 16.0)
             variants["bf16_logit_scale_16"] = summary(
-                measure_layer(layer, spec, min(args.steps, 5), 2, args.dense_steps, stream), spec, 16.0, "bf16")
+                measure_layer(layer, spec, vreps, 2, args.dense_steps, stream), spec, 16.0, "bf16")
             variants["bf16_logit_scale_16"]["selection_ablation"] = selection_ablation(layer, spec, stream)
-            layer.q.div_(16.0)
+            layer.params.mean_correction = 0
+            variants["bf16_logit_scale_16_mc_off"] = summary(
+                measure_layer(layer, spec, vreps, 2, 0, stream), spec, 16.0, "bf16", mean_corr=False)
+            layer.params.mean_correction = 1
+            variants["bf16_logit_scale_16"]["mean_correction_overhead_ms"] = round(
+                variants["bf16_logit_scale_16"]["stages_ms"]["sparse_attn"]
+                - variants["bf16_logit_scale_16_mc_off"]["stages_ms"]["sparse_attn"], 4)
+            scale_queries(layer, 1.0 / 16.0)
         del layer
         torch.cuda.empty_cache()
         spec8 = synth.config_spec(args.workload, dtype="e4m3")
         case8 = synth.make_case(spec8)
         layer8 = fprefill.layer_from_case(case8, device=dev)
-        variants["e4m3"] = summary(measure_layer(layer8, spec8, min(args.steps, 5), 2, args.dense_steps, stream,
-                                                 fp8=True), spec8, 1.0, "e4m3")
-        layer8.q_scale.mul_(16.0)               # the same sharper logits, exactly, through the scales
+        variants["e4m3"] = summary(measure_layer(layer8, spec8, vreps, 2, args.dense_steps, stream, fp8=True),
+                                   spec8, 1.0, "e4m3")
+        scale_queries(layer8, 16.0)             # the same sharper logits, exactly, through the scales
         variants["e4m3_logit_scale_16"] = summary(
-            measure_layer(layer8, spec8, min(args.steps, 5), 2, args.dense_steps, stream, fp8=True), spec8, 16.0,
-            "e4m3")
+            measure_layer(layer8, spec8, vreps, 2, args.dense_steps, stream, fp8=True), spec8, 16.0, "e4m3")
         del layer8, case8
         torch.cuda.empty_cache()
-        variants["bf16_chunk_512_at_128k"] = chunk_variant(dev, stream, min(args.steps, 5), args.dense_steps)
+        variants["bf16_chunk_512_at_128k"] = chunk_variant(dev, stream, vreps, args.dense_steps)
+        if args.other_workloads:
+            variants["llama8b_32k"] = workload_variants(2, dev, stream, vreps, args.dense_steps, mc_both=True)
+            variants["varlen_6req_chunk"] = workload_variants(4, dev, stream, vreps, args.dense_steps)
+        if args.sweep:
+            variants["density_error_sweep_256k"] = {
+                dt: density_error_sweep(dev, stream, dt, args.sweep_reps) for dt in ("bf16", "e4m3")}
+    else:
+        del layer
 
     peaks, peak_kind = load_peaks()
     attn_flop = stats["kept_flop"] + stats["corr_flop"]
@@ -386,13 +585,14 @@ def run_ours(args, rank, world):
         "data": "synthetic (seeded block-coherent Q/K with sink and needles, V ~ N(0,1))",
         "config": {"workload": spec.name, "batch": spec.batch, "seq_len": spec.total_q,
                    "h_q": spec.h_q, "h_kv": spec.h_kv, "d": spec.d, "page_size": spec.page_size,
-                   "page_layout": spec.layout, "alpha": 0.1, "sink_tokens": 256, "local_tokens": 512,
-                   "block": 128, "mean_correction": True, "logit_scale": args.logit_scale,
+                   "page_layout": spec.layout, "alpha": args.alpha, "sink_tokens": 256, "local_tokens": 512,
+                   "block": 128, "mean_correction": bool(args.mean_correction), "logit_scale": args.logit_scale,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2 (Q alone is {q_bytes / 2**20:.0f} MiB)"},
         "ms_per_layer": round(ms, 4),
         "stages_ms": {"discover": round(ms_disc, 4), "select": round(ms_sel, 4),
                       "sparse_attn": round(ms_attn, 4), "discover_select_fused": round(m["ms_dsel"], 4)},
+        "stages_timing": f"medians of {m['reps']} event-timed calls",
         "density": round(stats["density"], 5), "nnz_blocks": stats["nnz"], "csr_bytes": stats["csr_bytes"],
         "dense_attn_ms": None if ms_dense is None else round(ms_dense, 4),
         "speedup_vs_own_dense": None if ms_dense is None else round(ms_dense / ms, 3),
@@ -400,7 +600,7 @@ def run_ours(args, rank, world):
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic(spec, args.logit_scale),
                      "kernel": "attn_kernel (fp_sparse_attn)",
                      "peak_source": f"{peak_kind} bf16 sustained (MEASURED_PEAKS.json)" + (" x 2 for e4m3" if fp8 else "")},
-        "gpu_launches": (9 + (1 if layer_splits > 1 else 0)) * args.steps,
+        "gpu_launches": launches * args.steps,
         "device_status": status,
         "clocks": clocks,
         "gen_seconds": round(gen_s, 1),
@@ -439,11 +639,12 @@ def run_e2e(layer, steps, flop):
 # the float64 oracle on a bounded sample (CPU baseline and reference arm)
 # ----------------------------------------------------------------------------
 
-def oracle_sample(case, seconds: float, seed: int = 0):
+def oracle_sample(case, seconds: float, seed: int = 0, n_heads: int = 4):
     """Time the oracle's full path (pool, score, select, attention) on query
-    blocks of one kv head, adding blocks until `seconds` have elapsed; scale
-    by the share of the layer's work they represent (work of a row is
-    proportional to its causal length I+1)."""
+    blocks of `n_heads` sampled kv heads (all of them when the layer has no
+    more), adding blocks until `seconds` have elapsed; scale by the share of
+    the layer's work they represent (the work of a row is proportional to its
+    causal length I+1, and every kv head does the same work)."""
     import oracle
     spec = case.spec
     r = max(range(spec.batch), key=lambda x: spec.requests[x][0])
@@ -451,6 +652,7 @@ def oracle_sample(case, seconds: float, seed: int = 0):
     hkv, g, B = spec.h_kv, spec.h_q // spec.h_kv, 128
     nqb = -(-lq // B)
     rng = np.random.default_rng(seed)
+    heads = sorted(rng.choice(hkv, size=min(n_heads, hkv), replace=False).tolist())
     t_all = time.perf_counter()
     k, v = oracle.request_kv(case, r)            # decode (not counted as method work)
     t0 = time.perf_counter()
@@ -459,24 +661,24 @@ def oracle_sample(case, seconds: float, seed: int = 0):
     q0 = int(case.cu_seqlens_q[r])
     done_w, t_rows, nblocks = 0.0, 0.0, 0
     order = rng.permutation(nqb)
-    h = 0
     for i in order:
         rows = slice(i * B, min(lq, (i + 1) * B))
         qs = oracle.decode(case.q[q0 + rows.start:q0 + rows.stop], spec.dtype) * \
             case.q_scale.astype(np.float64)[None, :, None]
         I = start // B + i
         qstart = start + i * B            # the block seen as a request starting at its first query
-        t0 = time.perf_counter()
-        s = oracle.score_rows(qs, qstart, hkv, B, 1 / math.sqrt(spec.d), kbar, [h])[0]
-        keep_row, _ = oracle.select_row(s, I, 0.1, B, 256, 512)
-        keep = np.zeros((1, hkv, kbar.shape[0]), np.uint8)
-        keep[0, h, :I + 1] = keep_row
         n = rows.stop - rows.start
-        qi = np.repeat(np.arange(n), g)
-        qh = np.tile(np.arange(h * g, (h + 1) * g), n)
+        t0 = time.perf_counter()
+        srows = oracle.score_rows(qs, qstart, hkv, B, 1 / math.sqrt(spec.d), kbar, heads)
+        keep = np.zeros((1, hkv, kbar.shape[0]), np.uint8)
+        for h, s in zip(heads, srows):
+            keep_row, _ = oracle.select_row(s, I, 0.1, B, 256, 512)
+            keep[0, h, :I + 1] = keep_row
+        qi = np.repeat(np.arange(n), g * len(heads))
+        qh = np.tile(np.concatenate([np.arange(h * g, (h + 1) * g) for h in heads]), n)
         oracle.attn_rows(qs, qstart, k, v, kbar, vbar, B, 1 / math.sqrt(spec.d), keep, True, qi, qh)
         t_rows += time.perf_counter() - t0
-        done_w += (I + 1) * (rows.stop - rows.start)
+        done_w += (I + 1) * n * len(heads)
         nblocks += 1
         if time.perf_counter() - t_all > seconds:
             break
@@ -486,8 +688,8 @@ def oracle_sample(case, seconds: float, seed: int = 0):
     est_ms = (t_rows * total_w / done_w + t_pool * spec.total_k / k.shape[0]) * 1e3
     threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     return est_ms, dict(kind="oracle", cores=threads,
-                        sample=f"{nblocks} query blocks x 1 kv head of request {r} (full pooling), "
-                               f"scaled by causal work to the whole layer",
+                        sample=f"{nblocks} query blocks x {len(heads)} kv heads {heads} of request {r} "
+                               f"(full pooling), scaled by causal work to the whole layer",
                         sampled_seconds=round(t_rows + t_pool, 2))
 
 
@@ -527,11 +729,19 @@ def main():
     ap.add_argument("--logit-scale", type=float, default=1.0)
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3"],
                     help="arithmetic of the main workload (the variants run only with bf16)")
+    ap.add_argument("--alpha", type=float, default=0.1, help="threshold of the main workload")
+    ap.add_argument("--no-mean-correction", dest="mean_correction", action="store_false",
+                    help="main workload without the block-mean correction")
     ap.add_argument("--dense-steps", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-variants", dest="variants", action="store_false",
-                    help="skip the sparse-regime and FP8 variants")
+                    help="skip every variant (sparse regime, FP8, other workloads, sweep)")
+    ap.add_argument("--no-other-workloads", dest="other_workloads", action="store_false",
+                    help="skip the 32K layer and the varlen batch")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false",
+                    help="skip the 256K alpha x mean-correction density/error sweep")
+    ap.add_argument("--sweep-reps", type=int, default=3)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

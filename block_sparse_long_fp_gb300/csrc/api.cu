@@ -190,6 +190,19 @@ long long fp_score_size(const fp_problem *p, const fp_params *prm) {
     return build_desc(p, prm, &bd) == FP_OK ? bd.score_size : -1;
 }
 
+long long fp_score_offsets(const fp_problem *p, const fp_params *prm, long long *offsets, long long n) {
+    BatchDesc bd;
+    if (!offsets || build_desc(p, prm, &bd) != FP_OK || n < (long long)bd.total_rows + 1) return -1;
+    long long k = 0;
+    for (int r = 0; r < bd.batch; ++r) {
+        const ReqDesc &rq = bd.req[r];
+        for (int i = 0; i < rq.nqb; ++i)
+            for (int h = 0; h < bd.h_kv; ++h) offsets[k++] = score_row_offset(rq, bd.h_kv, i, h);
+    }
+    offsets[k] = bd.score_size;
+    return k + 1;
+}
+
 long long fp_total_q(const fp_problem *p) {
     if (!p || !p->cu_seqlens_q || p->batch < 1) return -1;
     return p->cu_seqlens_q[p->batch];

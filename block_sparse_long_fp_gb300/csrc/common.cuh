@@ -76,7 +76,7 @@ __device__ __forceinline__ int req_of_kb(const BatchDesc &bd, int kb) {
 }
 
 // Offset of score row (i, h) of request `rq` (the layout in fprefill.h).
-__device__ __forceinline__ long long score_row_offset(const ReqDesc &rq, int h_kv, int i, int h) {
+__host__ __device__ __forceinline__ long long score_row_offset(const ReqDesc &rq, int h_kv, int i, int h) {
     long long I0 = rq.start / kBlock;
     return rq.score_base + (long long)h_kv * (i * (I0 + 1) + (long long)i * (i - 1) / 2) +
            (long long)h * (I0 + i + 1);

@@ -11,7 +11,6 @@
 // FP_NOALLOC_SCRATCH_BYTES, reserved on every GPU that loads the library for
 // as long as the process lives.  The computation is exactly fp_sparse_attn's:
 // this file only supplies that array as its workspace.
-#include <mutex>
 #include <stdio.h>
 #include <stdlib.h>
 
@@ -23,28 +22,22 @@ static __device__ __align__(256) unsigned char fp_noalloc_scratch[FP_NOALLOC_SCR
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void *g_scratch_addr[kMaxDevices] = {nullptr};
-
-// Device address of the scratch array on the current device, looked up once
-// per device (with that device current) and cached.
-fp_status scratch_on_current_device(void **addr) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, fp_noalloc_scratch);
-        if (e != cudaSuccess || !p) {
-            const char *dbg = getenv("FPREFILL_DEBUG");
-            if (dbg && *dbg && *dbg != '0')
-                fprintf(stderr, "[fprefill] scratch address on device %d: %s\n", dev, cudaGetErrorString(e));
-            return FP_ERR_CUDA;
-        }
-        g_scratch_addr[dev] = p;
+// Device address of the scratch array in the caller's current context.  It
+// is looked up on every call and never cached: an address belongs to the
+// context it came from, and a caller may make a non-primary context current,
+// or reset the device (which destroys the context), between calls.  The
+// lookup is a host-side table read once the module is loaded; the first call
+// in a context may load it, which is why that call must come before any
+// stream capture.
+fp_status scratch_in_current_context(void **addr) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, fp_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+        const char *dbg = getenv("FPREFILL_DEBUG");
+        if (dbg && *dbg && *dbg != '0') fprintf(stderr, "[fprefill] scratch address: %s\n", cudaGetErrorString(e));
+        return FP_ERR_CUDA;
     }
-    *addr = g_scratch_addr[dev];
+    *addr = p;
     return FP_OK;
 }
 
@@ -74,7 +67,7 @@ extern "C" fp_status fp_sparse_attn_noalloc(const fp_problem *p, const fp_params
         return FP_ERR_WORKSPACE;
     }
     void *scratch = nullptr;
-    if ((s = scratch_on_current_device(&scratch)) != FP_OK) return s;
+    if ((s = scratch_in_current_context(&scratch)) != FP_OK) return s;
     // the array keeps the previous call's contents: the status word must start at zero
     if ((s = fp_reset_status(scratch, stream)) != FP_OK) return s;
     s = fp_sparse_attn(p, prm, row_ptr, col_idx, k_mean, v_mean, out, lse_opt, scratch, FP_NOALLOC_SCRATCH_BYTES,

@@ -64,6 +64,7 @@ def lib():
             "fp_num_key_blocks": ([P, PP], c_longlong),
             "fp_score_size": ([P, PP], c_longlong),
             "fp_total_q": ([P], c_longlong),
+            "fp_score_offsets": ([P, PP, c_void_p, c_longlong], c_longlong),
             "fp_discover_workspace_size": ([P, PP], c_size_t),
             "fp_discover": ([P, PP, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
             "fp_select_workspace_size": ([P, PP], c_size_t),
@@ -172,6 +173,15 @@ class Layer:
                             int(L.fp_discover_select_workspace_size(pp, pm)),
                             int(L.fp_attn_workspace_size(pp, pm)))
         self._ws = None
+
+    def score_offsets(self) -> np.ndarray:
+        """fp_score_offsets: int64 [rows + 1], the start of every score-map row
+        and, last, the map's size."""
+        offs = np.zeros(self.rows + 1, dtype=np.int64)
+        n = lib().fp_score_offsets(*self._refs(), offs.ctypes.data, offs.size)
+        if n != offs.size:
+            raise FprefillError(FP_ERR_INVALID, "fp_score_offsets")
+        return offs
 
     # -- plumbing -------------------------------------------------------------
     def _refs(self):

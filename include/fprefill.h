@@ -173,6 +173,13 @@ long long fp_num_key_blocks(const fp_problem *p, const fp_params *prm);  /* sum_
 long long fp_score_size(const fp_problem *p, const fp_params *prm);      /* floats in the score map */
 long long fp_total_q(const fp_problem *p);                               /* cu_seqlens_q[batch] */
 
+/* Offsets of the score-map rows (the closed form above), for callers that
+ * index the score map or the dense mask: offsets (HOST int64, n entries)
+ * receives the offset of row k = 0 .. R-1 in row order, then
+ * offsets[R] = fp_score_size().  Host-only: enqueues nothing.  Returns R + 1,
+ * or -1 when an argument is invalid or n < R + 1. */
+long long fp_score_offsets(const fp_problem *p, const fp_params *prm, long long *offsets, long long n);
+
 /* ---------------------------------------------------------------------------
  * fp_discover -- instantaneous pattern discovery
  * [V1 3.1 key pooling + query-block scoring; V2 4.1 block means of K and V]
@@ -288,9 +295,11 @@ fp_status fp_sparse_attn(const fp_problem *p, const fp_params *prm, const int *r
  *   Returns FP_ERR_WORKSPACE when the problem needs more scratch than
  *     FP_NOALLOC_SCRATCH_BYTES (compare fp_attn_workspace_size()), before
  *     touching the GPU; other argument errors as fp_sparse_attn.
- *   The first call on a device (with that device current) looks up the
- *     array's device address once and caches it; make that first call before
- *     any stream capture.
+ *   Every call looks up the array's device address in the caller's current
+ *     context (nothing is cached, so non-primary contexts and a device reset
+ *     between calls are fine).  The first call in a context may load the
+ *     library's device code into it: make that first call before any stream
+ *     capture.
  *   Every call on a device shares the one array, and the array keeps the last
  *   call's contents (the call clears what must start at zero).  Calls that
  *   overlap on the GPU -- on different streams, or from different threads --

@@ -64,6 +64,26 @@ def test_sizes_match_the_documented_layout(fp, oracle_mod):
     assert L.fp_attn_workspace_size(ctypes.byref(pr), ctypes.byref(prm)) >= 256 + rows * 4
 
 
+def test_score_offsets_follow_the_documented_layout(fp, oracle_mod):
+    """fp_score_offsets (host only) against the oracle's own restatement of
+    the score-map layout, on a varlen batch with chunks and a one-token request."""
+    reqs = [(300, 0), (1000, 0), (256, 512), (1, 128), (640, 0)]
+    pr, keep = problem(fp, reqs, h_q=8, h_kv=2)
+    prm = fp.default_params()
+    L = fp.lib()
+    rows = int(L.fp_num_rows(ctypes.byref(pr), ctypes.byref(prm)))
+    offs = np.full(rows + 1, -7, np.int64)
+    assert L.fp_score_offsets(ctypes.byref(pr), ctypes.byref(prm), offs.ctypes.data, offs.size) == rows + 1
+    ref, total = oracle_mod.score_row_offsets(reqs, 2, 128)
+    assert np.array_equal(offs[:-1], np.concatenate([o.reshape(-1) for o in ref]))
+    assert offs[-1] == total == L.fp_score_size(ctypes.byref(pr), ctypes.byref(prm))
+    # too small an array, or a null one, is refused without writing
+    small = np.full(rows, -7, np.int64)
+    assert L.fp_score_offsets(ctypes.byref(pr), ctypes.byref(prm), small.ctypes.data, small.size) == -1
+    assert np.all(small == -7)
+    assert L.fp_score_offsets(ctypes.byref(pr), ctypes.byref(prm), None, rows + 1) == -1
+
+
 def test_default_params_are_the_pages_configuration(fp):
     p = fp.default_params()
     assert (p.block, p.sink_tokens, p.local_tokens, p.mean_correction) == (128, 256, 512, 1)

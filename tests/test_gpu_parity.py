@@ -225,8 +225,12 @@ def test_topk_topp_on_a_ragged_varlen_batch(select):
 def test_discover_select_equals_the_separate_stages(name, select):
     """fp_discover_select gives bit for bit what fp_discover + fp_select give:
     the same means, score map and index (fused with the threshold rule; the
-    separate kernels behind one call for the other rules)."""
+    separate kernels behind one call for the other rules).  Its own outputs
+    are also checked against the oracle: the means, the optional score map,
+    and the index of both forms of the call (with and without the score map)
+    outside the flagged near-threshold band."""
     import torch
+    import oracle
     from block_sparse_long_fp_gb300 import fprefill
     specs = {
         "varlen": synth.Spec("varlen-small", [(300, 0), (1000, 0), (256, 512), (1, 128), (640, 0)], 8, 2,
@@ -237,7 +241,8 @@ def test_discover_select_equals_the_separate_stages(name, select):
                            n_needles=2, logit_scale=6.0, dtype="e4m3", config_id=94),
     }
     case = synth.make_case(specs[name])
-    layer = fprefill.layer_from_case(case, params=fprefill.default_params(**(select or {})))
+    sel = select or {}
+    layer = fprefill.layer_from_case(case, params=fprefill.default_params(**sel))
     km, vm, sc = layer.discover()
     rp, ci, nz = layer.select(sc)
     score = torch.full_like(sc, float("nan"))
@@ -251,6 +256,17 @@ def test_discover_select_equals_the_separate_stages(name, select):
     assert torch.equal(sc, score)
     assert torch.equal(rp, rp2) and torch.equal(rp, rp3)
     assert torch.equal(ci[:n], ci2[:n]) and torch.equal(ci[:n], ci3[:n])
+    # the fused call's own outputs against the float64 oracle
+    ref = oracle.discover_and_select(case, rule=sel.get("select_rule", 0), top_k=sel.get("top_k", 0),
+                                     top_p=sel.get("top_p", 0.0))
+    fused = dict(k_mean=km3.cpu().numpy(), v_mean=vm3.cpu().numpy(), score=None, row_ptr=rp3.cpu().numpy(),
+                 col_idx=ci3.cpu().numpy())
+    check_pool(case, fused, ref)
+    check_scores_and_index(case, fused, ref)
+    with_map = dict(k_mean=km2.cpu().numpy(), v_mean=vm2.cpu().numpy(), score=score.cpu().numpy(),
+                    row_ptr=rp2.cpu().numpy(), col_idx=ci2.cpu().numpy())
+    check_pool(case, with_map, ref)
+    check_scores_and_index(case, with_map, ref)
 
 
 @pytest.mark.parametrize("name", ["varlen", "sharp", "e4m3"])
@@ -351,27 +367,6 @@ def test_a_wait_that_runs_out_reports_timeout_and_the_context_stays_usable():
     torch.cuda.synchronize()
     assert layer.device_status() == 0
     assert torch.equal(out2, ref_out) and torch.equal(lse2, ref_lse)
-
-
-@pytest.mark.slow
-def test_llama8b_32k_sampled():
-    """Workload 2 (32K, 32/8 heads, shuffled 64-token pages): every pooled
-    block, a sample of score rows and of output rows."""
-    import oracle
-    spec = synth.config_spec(2)
-    case = synth.make_case(spec)
-    rng = np.random.default_rng(1)
-    sample = lambda r, nqb, hkv: np.unique(np.concatenate([rng.integers(0, nqb * hkv, 24),
-                                                           [0, nqb * hkv - 1]]))
-    ref = oracle.discover_and_select(case, row_subset=sample)
-    g = gpu_stage_outputs(case)
-    assert g["status"] == 0
-    check_pool(case, g, ref)
-    check_scores_and_index_sampled(case, g, ref)
-
-
-def check_scores_and_index_sampled(case, g, ref):
-    check_scores_and_index(case, g, ref)
 
 
 def test_fp8_discover_and_select():

@@ -83,3 +83,44 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
         assert torch.isfinite(out.float()).all(), f"call {call}"
         assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS, f"call {call}"
         assert (lse - ref_lse).abs().max().item() <= 2e-2, f"call {call}"
+
+
+@pytest.mark.gpu
+def test_noalloc_reports_a_device_error_and_the_next_call_starts_clean():
+    """The scratch array keeps the last call's contents, status word included.
+    A call whose index holds a block past the diagonal records
+    FP_ERR_DEVICE_BOUNDS, which status_dev_opt must report; the next call,
+    on a good index, must start from a clear status (FP_OK) and give
+    fp_sparse_attn's result."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_sparse_long_fp_gb300 import build, fprefill
+    build.build()
+    spec = synth.Spec("noalloc-err", [(512, 0), (300, 128)], 4, 2, page_size=64, layout="shuffled",
+                      n_needles=1, logit_scale=6.0, config_id=83)
+    case = synth.make_case(spec)
+    layer = fprefill.layer_from_case(case)
+    k_mean, v_mean, score = layer.discover()
+    row_ptr, col_idx, _ = layer.select(score)
+    ref, ref_lse = layer.sparse_attn(row_ptr, col_idx, k_mean, v_mean)
+    torch.cuda.synchronize()
+    assert layer.device_status() == fprefill.FP_OK
+    bad = col_idx.clone()
+    rp = row_ptr.cpu().numpy()
+    bad[int(rp[2 * spec.h_kv])] = 3             # row (I = 2, kv head 0): a block after its diagonal
+    out = torch.empty_like(ref)
+    lse = torch.empty_like(ref_lse)
+    status = torch.full((1,), -1, dtype=torch.int32, device=ref.device)
+    layer.sparse_attn_noalloc(row_ptr, bad, k_mean, v_mean, out, lse, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == fprefill.FP_ERR_DEVICE_BOUNDS
+    status.fill_(-1)
+    out.fill_(float("nan"))
+    layer.sparse_attn_noalloc(row_ptr, col_idx, k_mean, v_mean, out, lse, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == fprefill.FP_OK
+    err = (out.float() - ref.float()).abs()
+    assert torch.isfinite(out.float()).all()
+    assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS
+    assert (lse - ref_lse).abs().max().item() <= 2e-2
