@@ -150,7 +150,8 @@ size_t attn_part_lse_bytes(const BatchDesc &bd, int n_split) {
 size_t attn_ws_bytes(const BatchDesc &bd, int n_split) {
     size_t n = kWsHeaderBytes;
     n += attn_work_bytes(bd, n_split);
-    n += 2 * align_up((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2, 256);
+    // copies of the block means: the key means in two terms, the value means in one
+    n += 3 * align_up((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2, 256);
     n += attn_part_o_bytes(bd, n_split) + attn_part_lse_bytes(bd, n_split);
     return n;
 }
@@ -388,7 +389,7 @@ static fp_status run_attn(const fp_problem *p, const fp_params *prm, const int *
     L.work = reinterpret_cast<int *>(w + off);
     off += attn_work_bytes(bd, n_split);
     L.km16 = reinterpret_cast<__nv_bfloat16 *>(w + off);
-    off += align_up((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2, 256);
+    off += 2 * align_up((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2, 256);
     L.vm16 = reinterpret_cast<__nv_bfloat16 *>(w + off);
     off += align_up((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2, 256);
     L.n_split = n_split;

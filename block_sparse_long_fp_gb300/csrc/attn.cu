@@ -29,8 +29,17 @@
 //    one tile's softmax overlap the other tile's MMAs (the pingpong of V2
 //    section 4.2 (3), with TMEM accumulators instead of registers);
 //  * item list of a unit: the kept blocks (CSR row, ascending), then the
-//    128-wide tiles of block means that contain at least one skipped block;
-//    the dense path walks J = 0..I with no mean tiles.
+//    tiles of block means that contain at least one skipped block; the dense
+//    path walks J = 0..I with no mean tiles;
+//  * a mean token's logit goes into the exponent, and one bf16 term of the key
+//    means moves it by up to 2^-9 * scale * sum_c |q_c kmean_c| (e4m3: 2^-4),
+//    so the key means enter S as two terms, hi + lo.  An e4m3 mean tile packs
+//    both 16 KB terms of 128 blocks into its K slot, and its S takes 4 more
+//    MMAs.  A bf16 mean tile covers 64 blocks: K slot rows 0..63 hold their hi
+//    terms and rows 64..127 their lo terms, the S MMAs are those of any tile,
+//    and the softmax adds column c + 64 to column c.  (Extra MMA code in the
+//    MMA thread, wherever placed, made that thread spill around every MMA and
+//    slowed every launch, dense ones included, by 10-25%.)
 // Every mbarrier wait is bounded (status FP_ERR_TIMEOUT instead of a hang).
 #include <stdio.h>
 #include <stdlib.h>
@@ -59,7 +68,7 @@ constexpr int kSmemK = 2 * kTileBytes;
 constexpr int kSmemV = 4 * kTileBytes;
 constexpr int kSmemCtl = 6 * kTileBytes;                   // 192 KB
 constexpr int kBitmapWords = FP_MAX_KEY_BLOCKS / 32;
-constexpr int kMaxCorrTiles = FP_MAX_KEY_BLOCKS / kBlock;
+constexpr int kMaxCorrTiles = FP_MAX_KEY_BLOCKS / (kBlock / 2);   // bf16 mean tiles span 64 blocks
 
 // BAR_DR: the MMA thread's drain before the CTA leaves
 enum { BAR_Q = 0, BAR_QE = 1, BAR_KF = 2, BAR_KE = 4, BAR_VF = 6, BAR_VE = 8, BAR_SF = 10, BAR_PF = 12,
@@ -103,7 +112,7 @@ struct AttnArgs {
     float *part_o;            // n_split > 1: fp32 partial outputs [n_split, total_q, h_q, d]
     float *part_lse;          // n_split > 1: partial LSEs [n_split, h_q, total_q]
     int mean_corr;
-    int mean_rows;            // e4m3: row offset of the lo term of the key means
+    int mean_rows;            // row offset of the lo term of the key means
     float scale_log2;         // softmax scale * log2(e)
     const float *q_scale;     // e4m3 only: per query head / kv head scales
     const float *k_scale;
@@ -181,6 +190,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
     // e4m3 in one 128-column box; smem slots are 32 KB either way
     constexpr int kT = kFp8 ? kTileBytes / 2 : kTileBytes;
     constexpr int kNH = kFp8 ? 1 : 2;
+    constexpr int kMeanSpan = kFp8 ? kBlock : kBlock / 2;   // blocks per mean tile
     const bool sparse = a.row_ptr != nullptr;
 
     // ---- set-up (once per CTA) ---------------------------------------------------
@@ -250,13 +260,13 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                             if (J >= 0 && J < I) atomicOr(&M.bitmap[J >> 5], 1u << (J & 31));
                         }
                         __syncwarp();
-                        const int ntiles = (I + kBlock - 1) / kBlock;
+                        const int ntiles = (I + kMeanSpan - 1) / kMeanSpan;
                         for (int c0 = 0; c0 < ntiles; c0 += 32) {
                             const int c = c0 + lane;
                             bool any = false;
                             if (c < ntiles) {
-                                for (int w = 0; w < 4; ++w) {
-                                    const int J0 = c * kBlock + w * 32;
+                                for (int w = 0; w < kMeanSpan / 32; ++w) {
+                                    const int J0 = c * kMeanSpan + w * 32;
                                     if (J0 >= I) break;
                                     const uint32_t valid = (I - J0 >= 32) ? 0xffffffffu : ((1u << (I - J0)) - 1u);
                                     if (~M.bitmap[J0 >> 5] & valid) any = true;
@@ -437,12 +447,26 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                                             for (int hf = 0; hf < kNH; ++hf)
                                                 tma_load_3d(dst + hf * kHalfBytes + sub * rpb * 128, tm, full, hf * 64,
                                                             U.h, zs[sub]);
-                                } else {
+                                } else if (kFp8) {
+                                    // e4m3 mean tile: K slot <- hi, and lo in its upper half
                                     const CUtensorMap *tm = op == 0 ? &tmKm : &tmVm;
-                                    for (int hf = 0; hf < kNH; ++hf)
-                                        tma_load_3d(dst + hf * kHalfBytes, tm, full, hf * 64, U.h, rq.kb_base + c * kBlock);
+                                    tma_load_3d(dst, tm, full, 0, U.h, rq.kb_base + c * kBlock);
                                     if (two)
                                         tma_load_3d(dst + kHalfBytes, tm, full, 0, U.h, a.mean_rows + rq.kb_base + c * kBlock);
+                                } else {
+                                    // bf16 mean tile of 64 blocks: K slot rows 0..63 <- the hi terms
+                                    // of their key means, rows 64..127 <- the lo terms; V slot <- the
+                                    // value means (rows 64..127 get zero weight)
+                                    const int row0 = rq.kb_base + c * kMeanSpan;
+                                    for (int hf = 0; hf < kNH; ++hf) {
+                                        if (op == 0) {
+                                            tma_load_3d(dst + hf * kHalfBytes, &tmKm, full, hf * 64, U.h, row0);
+                                            tma_load_3d(dst + hf * kHalfBytes + kMeanSpan * 128, &tmKm, full, hf * 64, U.h,
+                                                        a.mean_rows + row0);
+                                        } else {
+                                            tma_load_3d(dst + hf * kHalfBytes, &tmVm, full, hf * 64, U.h, row0);
+                                        }
+                                    }
                                 }
                             }
                         }
@@ -672,19 +696,27 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                             if (k0 + e > pos) x[e] = -INFINITY;
                     }
                 } else {
-                    // mean tile c covers blocks 128c .. 128c+127; a skipped block J < I
-                    // is full (only the request's last block can be short, and
-                    // it is never before I), so its weight is n_J = 128: bias log2(128)
+                    // mean tile c covers blocks kMeanSpan*c .. +kMeanSpan-1; a skipped
+                    // block J < I is full (only the request's last block can be short,
+                    // and it is never before I), so its weight is n_J = 128: bias
+                    // log2(128).  bf16: column e < 64 holds q.hi of block 64c + e and
+                    // column e + 64 its q.lo
                     const int c = M.corr[j - n_kept];
-                    uint32_t w[4];
+                    uint32_t w[kMeanSpan / 32];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int J0 = c * kBlock + 32 * q;
+                    for (int q = 0; q < kMeanSpan / 32; ++q) {
+                        const int J0 = c * kMeanSpan + 32 * q;
                         uint32_t valid = J0 >= I ? 0u : (I - J0 >= 32 ? 0xffffffffu : ((1u << (I - J0)) - 1u));
                         w[q] = valid ? (~M.bitmap[J0 >> 5] & valid) : 0u;   // 1 = skipped, before I
                     }
+                    if constexpr (!kFp8) {
 #pragma unroll
-                    for (int e = 0; e < 128; ++e)
+                        for (int e = 0; e < 64; ++e) x[e] += x[e + 64];
+#pragma unroll
+                        for (int e = 64; e < 128; ++e) x[e] = -INFINITY;
+                    }
+#pragma unroll
+                    for (int e = 0; e < kMeanSpan; ++e)
                         if (!((w[e >> 5] >> (e & 31)) & 1u)) x[e] = -INFINITY;
                     bias = 7.f;
                 }
@@ -732,13 +764,21 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 uint32_t pk[kPk];
                 if constexpr (!kFp8) {
                     const uint64_t oo = f2_pack(off, off);
+                    // a mean tile's columns 64..127 (its lo terms, folded into 0..63)
+                    // carry no weight
+                    const bool lo_half = j >= n_kept;
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
+                        if (half == 1 && lo_half) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            float z0, z1;
-                            f2_unpack(f2_fma(f2_pack(x[64 * half + 2 * e], x[64 * half + 2 * e + 1]), cc, oo), z0, z1);
-                            pk[32 * half + e] = pack_bf16(fast_exp2(z0), fast_exp2(z1));
+                            for (int e = 0; e < 32; ++e) pk[32 + e] = 0u;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                float z0, z1;
+                                f2_unpack(f2_fma(f2_pack(x[64 * half + 2 * e], x[64 * half + 2 * e + 1]), cc, oo), z0, z1);
+                                pk[32 * half + e] = pack_bf16(fast_exp2(z0), fast_exp2(z1));
+                            }
                         }
                         tmem_st32(tS + 32 * half, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * half));
                     }
@@ -899,7 +939,7 @@ constexpr int kSchedThreads = 1024;
 
 __global__ void __launch_bounds__(kSchedThreads)
 sched_kernel(const __grid_constant__ BatchDesc bd, const int *__restrict__ row_ptr, int n_pairs, int n_split,
-             int mean_corr, int *__restrict__ work, int *__restrict__ next_unit) {
+             int mean_span, int *__restrict__ work, int *__restrict__ next_unit) {
     __shared__ int hist[kSchedBins];
     __shared__ int warp_sum[kSchedThreads / 32];
     __shared__ int grp[3];                          // request, kv head, first position of the group
@@ -931,7 +971,8 @@ sched_kernel(const __grid_constant__ BatchDesc bd, const int *__restrict__ row_p
     auto cost = [&](int il) {
         const int row = rq.row_base + il * bd.h_kv + h;
         const int I = rq.start / kBlock + il;
-        const int c = row_ptr ? row_ptr[row + 1] - row_ptr[row] + (mean_corr ? (I + kBlock - 1) / kBlock : 0) : I + 1;
+        const int c = row_ptr ? row_ptr[row + 1] - row_ptr[row] + (mean_span ? (I + mean_span - 1) / mean_span : 0)
+                              : I + 1;
         return kSchedBins - 1 - min(c, kSchedBins - 1);     // bin 0 = the most work
     };
     for (int il = tid; il < rq.nqb; il += kSchedThreads) atomicAdd(&hist[cost(il)], 1);
@@ -1011,13 +1052,18 @@ combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_
     if (lse && lane == 0) lse[(long long)head * total_q + tok] = den > 0.f ? mx + __logf(den) : -INFINITY;
 }
 
-// fp32 block means -> bf16 operands of the mean tiles; [n, n_pad) is zeroed
+// fp32 block means -> bf16 operands of the mean tiles; [n, n_pad) is zeroed.
+// The key means get two terms, hi at ao[k] and lo = bf16(x - hi) at
+// ao[n_pad + k] (16 significant bits together); the value means one.
 __global__ void to_bf16_kernel(const float *__restrict__ a, const float *__restrict__ b,
                                __nv_bfloat16 *__restrict__ ao, __nv_bfloat16 *__restrict__ bo, long long n,
                                long long n_pad) {
     for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n_pad;
          k += (long long)gridDim.x * blockDim.x) {
-        ao[k] = __float2bfloat16_rn(k < n ? a[k] : 0.f);
+        const float x = k < n ? a[k] : 0.f;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+        ao[k] = hi;
+        ao[n_pad + k] = __float2bfloat16_rn(x - __bfloat162float(hi));
         bo[k] = __float2bfloat16_rn(k < n ? b[k] : 0.f);
     }
 }
@@ -1177,9 +1223,10 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
         else
             to_bf16_kernel<<<1024, 256, 0, st>>>(L.k_mean, L.v_mean, L.km16, L.vm16, n, n_pad);
         if ((e = cudaGetLastError()) != cudaSuccess) return fail("mean conversion launch", (int)e);
-        // e4m3: hi rows [0, mean_rows), lo rows [mean_rows, 2 mean_rows)
-        if (!make_map(&tmKm, L.km16, bd.h_kv, (f8 ? 2LL : 1LL) * mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim,
-                      kBlock, f8))
+        // the key means' hi rows [0, mean_rows), lo rows [mean_rows, 2 mean_rows);
+        // bf16 mean tiles load each term as 64-row boxes
+        if (!make_map(&tmKm, L.km16, bd.h_kv, 2LL * mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim,
+                      f8 ? kBlock : kBlock / 2, f8))
             return fail("mean K map", 0);
         if (!make_map(&tmVm, L.vm16, bd.h_kv, mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock, f8))
             return fail("mean V map", 0);
@@ -1188,8 +1235,9 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
         tmVm = tmV;
     }
     int *next_unit = L.work + units;
-    sched_kernel<<<bd.batch * bd.h_kv, kSchedThreads, 0, st>>>(bd, L.row_ptr, n_pairs, n_split, use_means ? 1 : 0,
-                                                              L.work, next_unit);
+    const int mean_span = use_means ? (f8 ? kBlock : kBlock / 2) : 0;
+    sched_kernel<<<bd.batch * bd.h_kv, kSchedThreads, 0, st>>>(bd, L.row_ptr, n_pairs, n_split, mean_span, L.work,
+                                                              next_unit);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail("schedule launch", (int)e);
     AttnArgs a;
     a.row_ptr = L.row_ptr;

@@ -198,16 +198,16 @@ def test_split_kv_chunk_at_the_end_of_a_long_context(dtype, logit_scale):
                 lse_abs=FP8_LSE_ABS if fp8 else 2e-2)
 
 
-@pytest.mark.parametrize("select,mean_corr", [(dict(select_rule=1, top_k=1), False), (dict(select_rule=1, top_k=8), True),
+@pytest.mark.parametrize("select,mean_corr", [(dict(select_rule=1, top_k=1), True), (dict(select_rule=1, top_k=1), False),
+                                              (dict(select_rule=1, top_k=8), True),
                                               (dict(select_rule=2, top_p=0.5), True),
                                               (dict(select_rule=2, top_p=0.9), True)])
 def test_topk_topp_selection_ablations(select, mean_corr):
     """The top-k and top-p rules (ablations of the max threshold): the GPU's
     index equals the oracle's outside the flagged boundary band, and the
-    attention on it matches.  With one kept block per row a row is nearly all
-    mean tokens, whose keys enter the bf16 MMA rounded to bf16 (a logit error
-    up to 2^-9 * scale * sum_c |q_c kmean_c|, ~0.09 here): that case checks
-    the attention without the correction, exact over the kept blocks."""
+    attention on it matches.  With one kept block per row (k = 1) a row is
+    nearly all mean tokens: the mean tiles' keys enter the MMA as two bf16
+    terms, so their logits keep the accuracy of the kept blocks'."""
     spec = synth.Spec("sharp-8k", [(8192, 0)], 4, 1, page_size=64, layout="shuffled", n_needles=2,
                       logit_scale=8.0, config_id=1)
     full_parity(spec, rows_per_request=1500, select=select, mean_corr=mean_corr)
