@@ -225,7 +225,7 @@ def launches_per_step(layer) -> int:
     return 3 + SELECT_LAUNCHES + (mc + 2) + (1 if layer.kv_splits > 1 else 0)
 
 
-SELECT_LAUNCHES = 3
+SELECT_LAUNCHES = 1
 
 
 def measure_layer(layer, spec, reps, warmup, dense_reps, stream, fp8=False):

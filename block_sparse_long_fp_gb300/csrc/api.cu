@@ -252,7 +252,7 @@ fp_status fp_discover(const fp_problem *p, const fp_params *prm, float *k_mean, 
 size_t fp_select_workspace_size(const fp_problem *p, const fp_params *prm) {
     BatchDesc bd;
     if (build_desc(p, prm, &bd) != FP_OK) return 0;
-    return kWsHeaderBytes + align_up((size_t)bd.total_rows * sizeof(int), 256);
+    return kWsHeaderBytes + align_up(select_state_bytes(bd), 256);
 }
 
 fp_status fp_select(const fp_problem *p, const fp_params *prm, const float *score, int *row_ptr, int *col_idx,
@@ -266,9 +266,9 @@ fp_status fp_select(const fp_problem *p, const fp_params *prm, const float *scor
     if (!ws || ws_bytes < fp_select_workspace_size(p, prm)) return FP_ERR_WORKSPACE;
     const int sink_blocks = (prm->sink_tokens + kBlock - 1) / kBlock;
     const int local_blocks = (prm->local_tokens + kBlock - 1) / kBlock;
-    int *counts = reinterpret_cast<int *>(static_cast<char *>(ws) + kWsHeaderBytes);
+    void *lb_state = static_cast<char *>(ws) + kWsHeaderBytes;
     if (launch_select(bd, prm->alpha, sink_blocks, local_blocks, prm->select_rule, prm->top_k, prm->top_p, score,
-                      counts, row_ptr, col_idx, col_capacity, nnz_dev, dense_mask_opt, status_ptr(ws),
+                      lb_state, row_ptr, col_idx, col_capacity, nnz_dev, dense_mask_opt, status_ptr(ws), g_wait_ns,
                       (cudaStream_t)stream) != cudaSuccess)
         return FP_ERR_CUDA;
     return FP_OK;
@@ -335,7 +335,7 @@ fp_status fp_discover_select(const fp_problem *p, const fp_params *prm, float *k
                : launch_score(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean, scale, sc, st);
         if (e == cudaSuccess)
             e = launch_select(bd, prm->alpha, sink_blocks, local_blocks, prm->select_rule, prm->top_k, prm->top_p, sc,
-                              counts, row_ptr, col_idx, col_capacity, nnz_dev, nullptr, status_ptr(ws), st);
+                              counts, row_ptr, col_idx, col_capacity, nnz_dev, nullptr, status_ptr(ws), g_wait_ns, st);
     }
     return e == cudaSuccess ? FP_OK : FP_ERR_CUDA;
 }

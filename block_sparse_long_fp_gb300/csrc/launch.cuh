@@ -11,9 +11,12 @@ cudaError_t launch_pool(const BatchDesc &bd, bool fp8, const void *k_cache, cons
 cudaError_t launch_score(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
                          long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
                          float *score, cudaStream_t st);
+// lb_state: look-back scratch of select_state_bytes(bd), 8-byte aligned
 cudaError_t launch_select(const BatchDesc &bd, float alpha, int sink_blocks, int local_blocks, int rule, int top_k,
-                          float top_p, const float *score, int *counts, int *row_ptr, int *col_idx,
-                          long long col_capacity, int *nnz, unsigned char *dense_mask, int *status, cudaStream_t st);
+                          float top_p, const float *score, void *lb_state, int *row_ptr, int *col_idx,
+                          long long col_capacity, int *nnz, unsigned char *dense_mask, int *status,
+                          unsigned long long wait_ns, cudaStream_t st);
+inline size_t select_state_bytes(const BatchDesc &bd) { return (size_t)((bd.total_rows + 7) / 8 + 1) * 8; }
 size_t score_smem_bytes(int max_nkb);
 // tensor-core score map (bf16 inputs): the three bf16 terms of the means live in
 // a workspace of score_tc_terms_bytes()

@@ -5,13 +5,17 @@
 // jump"; V2 section 4 CSR output).  The top-k and top-p rules the V1 summary
 // (section 4.4) compares the threshold with are kept as ablations.
 //
-// Three launches, no host synchronisation: (1) one warp per row decides and
-// counts, (2) one CTA scans the counts into row_ptr, (3) one warp per row
-// repeats the identical decision and writes its kept blocks at row_ptr[row].
+// One launch, no host synchronisation: one warp per row decides and counts;
+// each CTA of eight rows learns the kept count of all earlier rows by a
+// decoupled look-back over the CTAs' published totals (a bounded wait); then
+// each warp writes row_ptr and its kept blocks at row_ptr[row].
 #include <limits.h>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "launch.cuh"
+#include "sm100.cuh"
 
 namespace fp {
 
@@ -115,29 +119,185 @@ __device__ __forceinline__ bool keep_block(float s, const RowRule &rr, int J, in
     return s > rr.t || (s == rr.t && J <= rr.jt) || J < a.sink_blocks || J >= I - a.local_blocks + 1;
 }
 
+// Look-back state of one CTA: bits [62, 64) status (0: nothing yet, 1: the
+// CTA's own total, 2: the inclusive total of all rows up to its last), [32,
+// 62) the call's epoch (a state left by an earlier call reads as nothing
+// yet, so the array needs no clearing), [0, 32) the value.
+constexpr unsigned long long kLbAgg = 1ull << 62, kLbPrefix = 2ull << 62;
+__device__ __forceinline__ unsigned long long lb_word(unsigned long long status, unsigned epoch, int v) {
+    return status | ((unsigned long long)(epoch & 0x3fffffffu) << 32) | (unsigned)v;
+}
+__device__ __forceinline__ void lb_publish(unsigned long long *p, unsigned long long w) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ unsigned long long lb_read(const unsigned long long *p) {
+    unsigned long long w;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+
+constexpr int kRegRow = 1024;      // rows of up to this many blocks decide from registers
+
 __global__ void __launch_bounds__(256)
-select_count_kernel(const __grid_constant__ BatchDesc bd, SelectArgs a, const float *__restrict__ score,
-                    int *__restrict__ counts, unsigned char *__restrict__ dense_mask) {
-    const int row = blockIdx.x * 8 + threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
-    if (row >= bd.total_rows) return;
-    const int r = req_of_row(bd, row);
-    const ReqDesc &rq = bd.req[r];
-    const int local = row - rq.row_base;
-    const int i = local / bd.h_kv, h = local % bd.h_kv;
-    const int I = rq.start / kBlock + i;
-    const long long off = score_row_offset(rq, bd.h_kv, i, h);
-    const float *s = score + off;
-    const RowRule rr = row_rule(s, I + 1, lane, a);
-    int cnt = 0;
-    for (int J = lane; J <= I; J += 32) {
-        bool k = keep_block(__ldg(s + J), rr, J, I, a);
-        cnt += k;
-        if (dense_mask) dense_mask[off + J] = (unsigned char)k;
-    }
+select_kernel(const __grid_constant__ BatchDesc bd, SelectArgs a, const float *__restrict__ score,
+              unsigned long long *__restrict__ lb_state, unsigned epoch, int *__restrict__ row_ptr,
+              int *__restrict__ col_idx, long long col_capacity, int *__restrict__ nnz,
+              unsigned char *__restrict__ dense_mask, int *status, unsigned long long wait_ns) {
+    __shared__ int cnt[8];
+    __shared__ int cta_base;
+    const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int row = blockIdx.x * 8 + w;
+    const bool have = row < bd.total_rows;
+    int I = 0, c = 0;
+    long long off = 0;
+    RowRule rr{0.f, INT_MAX};
+    // threshold rule on a row of at most kRegRow blocks: the row is read once,
+    // 32 scores per lane in registers (all loads in flight at once), and the
+    // maximum, the count and the compaction work from there; keep bit k of
+    // `kept` = block 32 k + lane
+    const bool in_regs = a.rule == FP_SELECT_THRESHOLD;
+    uint32_t kept = 0u;
+    if (have) {
+        const int r = req_of_row(bd, row);
+        const ReqDesc &rq = bd.req[r];
+        const int local = row - rq.row_base;
+        const int i = local / bd.h_kv, h = local % bd.h_kv;
+        I = rq.start / kBlock + i;
+        off = score_row_offset(rq, bd.h_kv, i, h);
+        const float *s = score + off;
+        if (in_regs && I < kRegRow) {
+            float v[32];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    if (lane == 0) counts[row] = cnt;
+            for (int k = 0; k < 32; ++k) {
+                const int J = 32 * k + lane;
+                v[k] = J <= I ? __ldg(s + J) : -INFINITY;
+            }
+            float mx = v[0];
+#pragma unroll
+            for (int k = 1; k < 32; ++k) mx = fmaxf(mx, v[k]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            rr.t = a.alpha * mx;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const int J = 32 * k + lane;
+                const bool kb = J <= I && keep_block(v[k], rr, J, I, a);
+                kept |= (uint32_t)kb << k;
+                if (dense_mask && J <= I) dense_mask[off + J] = (unsigned char)kb;
+            }
+            c = __popc(kept);
+        } else {
+            rr = row_rule(s, I + 1, lane, a);
+            for (int J = lane; J <= I; J += 32) {
+                const bool k = keep_block(__ldg(s + J), rr, J, I, a);
+                c += k;
+                if (dense_mask) dense_mask[off + J] = (unsigned char)k;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    }
+    if (lane == 0) cnt[w] = c;
+    __syncthreads();
+    if (w == 0) {
+        int agg = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) agg += cnt[k];
+        int excl = 0;
+        if (blockIdx.x > 0) {
+            if (lane == 0) lb_publish(lb_state + blockIdx.x, lb_word(kLbAgg, epoch, agg));
+            // warp-wide look-back over windows of 128 earlier CTAs: lane L reads
+            // CTAs end - (32 q + L), q = 0..3, all four loads in flight; the
+            // nearest CTA with an inclusive total ends the walk and the CTAs
+            // between that published their own totals are added; a window of
+            // 128 own totals moves the window back (bounded like every wait here)
+            const uint64_t t0 = sm100::global_ns();
+            for (int end = blockIdx.x - 1;;) {
+                unsigned long long st[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int b = end - 32 * q - lane;
+                    st[q] = b >= 0 ? lb_read(lb_state + b) : lb_word(kLbPrefix, epoch, 0);
+                }
+                bool done = false, step = true;
+                int add = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const bool mine = ((st[q] >> 32) & 0x3fffffffu) == (epoch & 0x3fffffffu);
+                    const unsigned kind = mine ? (unsigned)(st[q] >> 62) : 0u;   // 0: not yet published
+                    const int val = (int)(unsigned)st[q];
+                    const unsigned pre = __ballot_sync(0xffffffffu, kind == 2u);
+                    const unsigned rdy = __ballot_sync(0xffffffffu, kind != 0u);
+                    if (!done && step) {
+                        if (pre) {
+                            const int pl = __ffs(pre) - 1;                           // nearest inclusive total
+                            const unsigned need = pl == 31 ? 0xffffffffu : ((2u << pl) - 1u);
+                            if ((rdy & need) == need) {
+                                add += lane <= pl ? val : 0;
+                                done = true;
+                            } else {
+                                step = false;                                        // not all published yet
+                            }
+                        } else if (rdy == 0xffffffffu) {
+                            add += val;
+                        } else {
+                            step = false;
+                        }
+                    }
+                }
+                if (done || step) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) add += __shfl_xor_sync(0xffffffffu, add, o);
+                    excl += add;
+                    if (done) break;
+                    end -= 128;
+                    continue;
+                }
+                if (__any_sync(0xffffffffu, sm100::global_ns() - t0 > wait_ns)) {   // warp-uniform
+                    if (lane == 0) set_status(status, FP_ERR_TIMEOUT);
+                    break;
+                }
+            }
+        }
+        if (lane == 0) {
+            lb_publish(lb_state + blockIdx.x, lb_word(kLbPrefix, epoch, excl + agg));
+            cta_base = excl;
+        }
+    }
+    __syncthreads();
+    if (!have) return;
+    int pos = cta_base;
+    for (int k = 0; k < w; ++k) pos += cnt[k];
+    if (lane == 0) {
+        row_ptr[row] = pos;
+        if (row == bd.total_rows - 1) {
+            row_ptr[row + 1] = pos + c;
+            *nnz = pos + c;
+        }
+    }
+    if ((long long)pos + c > col_capacity) {
+        if (lane == 0) set_status(status, FP_ERR_INVALID);
+        return;
+    }
+    if (in_regs && I < kRegRow) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            if (32 * k > I) break;
+            const bool kb = (kept >> k) & 1u;
+            const unsigned m = __ballot_sync(0xffffffffu, kb);
+            if (kb) col_idx[pos + __popc(m & ((1u << lane) - 1u))] = 32 * k + lane;
+            pos += __popc(m);
+        }
+        return;
+    }
+    const float *s = score + off;
+    for (int J0 = 0; J0 <= I; J0 += 32) {
+        const int J = J0 + lane;
+        const bool k = J <= I && keep_block(__ldg(s + J), rr, J, I, a);
+        const unsigned m = __ballot_sync(0xffffffffu, k);
+        if (k) col_idx[pos + __popc(m & ((1u << lane) - 1u))] = J;
+        pos += __popc(m);
+    }
 }
 
 // Exclusive scan of the row counts into row_ptr[0..n], nnz = row_ptr[n]; row
@@ -187,34 +347,6 @@ scan_kernel(const int *__restrict__ counts, int n, int per_row, int *__restrict_
     }
 }
 
-__global__ void __launch_bounds__(256)
-select_compact_kernel(const __grid_constant__ BatchDesc bd, SelectArgs a, const float *__restrict__ score,
-                      const int *__restrict__ row_ptr, int *__restrict__ col_idx,
-                      long long col_capacity, int *status) {
-    const int row = blockIdx.x * 8 + threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
-    if (row >= bd.total_rows) return;
-    const int r = req_of_row(bd, row);
-    const ReqDesc &rq = bd.req[r];
-    const int local = row - rq.row_base;
-    const int i = local / bd.h_kv, h = local % bd.h_kv;
-    const int I = rq.start / kBlock + i;
-    const float *s = score + score_row_offset(rq, bd.h_kv, i, h);
-    const RowRule rr = row_rule(s, I + 1, lane, a);
-    int pos = row_ptr[row];
-    if ((long long)row_ptr[row + 1] > col_capacity) {
-        if (lane == 0) set_status(status, FP_ERR_INVALID);
-        return;
-    }
-    for (int J0 = 0; J0 <= I; J0 += 32) {
-        int J = J0 + lane;
-        bool k = J <= I && keep_block(__ldg(s + J), rr, J, I, a);
-        unsigned m = __ballot_sync(0xffffffffu, k);
-        if (k) col_idx[pos + __popc(m & ((1u << lane) - 1u))] = J;
-        pos += __popc(m);
-    }
-}
-
 // fused path: row warp w of the score kernel wrote the kept blocks of segment
 // w of the row at keep_pad[row offset + w * score_segment(I + 1)], and their
 // count at counts8[row * 8 + w]; after the scan, one warp per row joins the
@@ -255,14 +387,20 @@ cudaError_t launch_select_gather(const BatchDesc &bd, const int *keep_pad, const
 }
 
 cudaError_t launch_select(const BatchDesc &bd, float alpha, int sink_blocks, int local_blocks, int rule,
-                          int top_k, float top_p, const float *score, int *counts, int *row_ptr, int *col_idx,
+                          int top_k, float top_p, const float *score, void *lb_state, int *row_ptr, int *col_idx,
                           long long col_capacity, int *nnz, unsigned char *dense_mask, int *status,
-                          cudaStream_t st) {
+                          unsigned long long wait_ns, cudaStream_t st) {
     SelectArgs a{alpha, sink_blocks, local_blocks, rule, top_k, top_p};
-    int grid = (bd.total_rows + 7) / 8;
-    select_count_kernel<<<grid, 256, 0, st>>>(bd, a, score, counts, dense_mask);
-    scan_kernel<<<1, 1024, 0, st>>>(counts, bd.total_rows, 1, row_ptr, nnz);
-    select_compact_kernel<<<grid, 256, 0, st>>>(bd, a, score, row_ptr, col_idx, col_capacity, status);
+    if (bd.total_rows == 0) {
+        if (cudaMemsetAsync(row_ptr, 0, sizeof(int), st) != cudaSuccess) return cudaGetLastError();
+        return cudaMemsetAsync(nnz, 0, sizeof(int), st);
+    }
+    // a new epoch per call: look-back states of earlier calls read as empty
+    static std::atomic<unsigned> calls{0};
+    const unsigned epoch = (calls.fetch_add(1u) % 0x3ffffffeu) + 1u;
+    const int grid = (bd.total_rows + 7) / 8;
+    select_kernel<<<grid, 256, 0, st>>>(bd, a, score, static_cast<unsigned long long *>(lb_state), epoch, row_ptr,
+                                        col_idx, col_capacity, nnz, dense_mask, status, wait_ns);
     return cudaGetLastError();
 }
 
