@@ -559,6 +559,14 @@ def run_ours(args, rank, world):
         scale_queries(layer8, 16.0)             # the same sharper logits, exactly, through the scales
         variants["e4m3_logit_scale_16"] = summary(
             measure_layer(layer8, spec8, vreps, 2, args.dense_steps, stream, fp8=True), spec8, 16.0, "e4m3")
+        # P in two e4m3 terms (the residual through a second PV pass): the precise form
+        layer8.params.p_terms = 2
+        variants["e4m3_logit_scale_16_p_terms_2"] = summary(
+            measure_layer(layer8, spec8, vreps, 2, args.dense_steps, stream, fp8=True), spec8, 16.0, "e4m3")
+        scale_queries(layer8, 1.0 / 16.0)
+        variants["e4m3_p_terms_2"] = summary(
+            measure_layer(layer8, spec8, vreps, 2, args.dense_steps, stream, fp8=True), spec8, 1.0, "e4m3")
+        layer8.params.p_terms = 1
         del layer8, case8
         torch.cuda.empty_cache()
         variants["bf16_chunk_512_at_128k"] = chunk_variant(dev, stream, vreps, args.dense_steps)

@@ -32,6 +32,7 @@ fp_status build_desc(const fp_problem *p, const fp_params *prm, BatchDesc *bd) {
     if (prm->select_rule == FP_SELECT_TOPP && !(prm->top_p > 0.f && prm->top_p <= 1.f)) return FP_ERR_INVALID;
     if (prm->select_rule < FP_SELECT_THRESHOLD || prm->select_rule > FP_SELECT_TOPP) return FP_ERR_INVALID;
     if (prm->score_mode != FP_SCORE_PACKED && prm->score_mode != FP_SCORE_HEAD_UNION) return FP_ERR_INVALID;
+    if (prm->p_terms < 0 || prm->p_terms > 2) return FP_ERR_INVALID;
     memset(bd, 0, sizeof(*bd));
     bd->batch = p->batch;
     bd->h_q = p->h_q;
@@ -173,6 +174,7 @@ fp_params fp_default_params(void) {
     p.top_k = 0;
     p.top_p = 0.f;
     p.score_mode = FP_SCORE_PACKED;
+    p.p_terms = 1;
     return p;
 }
 
@@ -399,6 +401,7 @@ static fp_status run_attn(const fp_problem *p, const fp_params *prm, const int *
     L.wait_ns = g_wait_ns;
     L.fp8 = p->dtype == FP_E4M3;
     L.v_dim_major = p->v_layout == FP_V_DIM_MAJOR;
+    L.p_terms = prm->p_terms == 2 ? 2 : 1;
     L.q_scale = p->q_scale;
     L.k_scale = p->k_scale;
     L.v_scale = p->v_scale;

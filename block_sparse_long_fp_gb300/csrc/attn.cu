@@ -170,7 +170,11 @@ __device__ __forceinline__ Unit decode_unit(const BatchDesc &bd, const AttnArgs 
 // LSE or rows are split; it costs ~10% of the e4m3 kernel)
 // kVdm: the value cache is dim-major ([num_pages, h_kv, d, page_size]): a kept
 // block's V tile arrives as d rows of keys and is a K-major operand of PV
-template <bool kFp8, bool kLse, bool kVdm>
+// kPlo (e4m3 only): P enters PV in two e4m3 terms, hi = e4m3(256 p) and the
+// residual lo = e4m3(256 p - hi) in the next 32 TMEM columns, through a second
+// PV pass: e4m3's 1/16 relative rounding of the largest weights drops to
+// about 1/256
+template <bool kFp8, bool kLse, bool kVdm, bool kPlo = false>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtensorMap tmQ,
             const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -426,8 +430,9 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                                     break;
                                 }
                                 const uint32_t dst = sbase + (op == 0 ? kSmemK : kSmemV) + s * kTileBytes;
-                                // e4m3 mean K tiles carry a second (lo) term in the slot's upper half
-                                const bool two = kFp8 && !kept && op == 0;
+                                // e4m3 mean K tiles carry a second (lo) term in the slot's upper half;
+                                // kPlo V tiles arrive twice (both halves of the slot)
+                                const bool two = (kFp8 && !kept && op == 0) || (kPlo && op == 1);
                                 mbar_expect_tx(full, two ? 2 * kT : kT);
                                 if (kept && kVdm && op == 1) {
                                     // d rows of 128 / esz keys per box (K-major): bf16 as two
@@ -438,21 +443,28 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                                         const int z = zs[(hf * 64) / rpb] + (hf * 64) % rpb;
                                         tma_load_3d(dst + hf * kHalfBytes, &tmV, full, z % a.page_size, U.h * kHeadDim,
                                                     z / a.page_size);
+                                        if (kPlo)
+                                            tma_load_3d(dst + kT, &tmV, full, z % a.page_size, U.h * kHeadDim, z / a.page_size);
                                     }
                                 } else if (kept) {
                                     const CUtensorMap *tm = op == 0 ? &tmK : &tmV;
 #pragma unroll
                                     for (int sub = 0; sub < 8; ++sub)
                                         if (sub < nsub)
-                                            for (int hf = 0; hf < kNH; ++hf)
+                                            for (int hf = 0; hf < kNH; ++hf) {
                                                 tma_load_3d(dst + hf * kHalfBytes + sub * rpb * 128, tm, full, hf * 64,
                                                             U.h, zs[sub]);
+                                                if (kPlo && op == 1)
+                                                    tma_load_3d(dst + kT + sub * rpb * 128, tm, full, 0, U.h, zs[sub]);
+                                            }
                                 } else if (kFp8) {
-                                    // e4m3 mean tile: K slot <- hi, and lo in its upper half
+                                    // e4m3 mean tile: K slot <- hi, and lo in its upper half; V slot
+                                    // <- the value means (twice with kPlo)
                                     const CUtensorMap *tm = op == 0 ? &tmKm : &tmVm;
                                     tma_load_3d(dst, tm, full, 0, U.h, rq.kb_base + c * kBlock);
                                     if (two)
-                                        tma_load_3d(dst + kHalfBytes, tm, full, 0, U.h, a.mean_rows + rq.kb_base + c * kBlock);
+                                        tma_load_3d(dst + kHalfBytes, tm, full, 0, U.h,
+                                                    (op == 0 ? a.mean_rows : 0) + rq.kb_base + c * kBlock);
                                 } else {
                                     // bf16 mean tile of 64 blocks: K slot rows 0..63 <- the hi terms
                                     // of their key means, rows 64..127 <- the lo terms; V slot <- the
@@ -524,12 +536,16 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             // kept: a kept block's tile, K-major when the value cache is dim-major
             // (the same descriptors and steps as the K operand of S); mean tiles
             // and token-major tiles are MN-major
+            // kPlo: 256 virtual keys, A = [P_hi | P_lo] (TMEM columns 0..63) against
+            // B = [V; V] (the slot holds the e4m3 tile twice)
+            constexpr int kPvSteps = kPlo ? 2 * kKSteps : kKSteps;
             auto issue_PV = [&](int t, int s, bool acc, bool kept) {
                 if (kVdm && kept) {
                     const uint64_t vd = kvdesc + ((s * kTileBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kKSteps; ++kk) {
-                        const uint32_t off = (kFp8 ? kk * 32 : (kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                    for (int kk = 0; kk < kPvSteps; ++kk) {
+                        const uint32_t off =
+                            (kFp8 ? (kk >> 2) * kT + (kk & 3) * 32 : (kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
                         if constexpr (kFp8) mma_ts_f8(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, vd + off, idS, (acc || kk > 0));
                         else mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, vd + off, idS, (acc || kk > 0));
                     }
@@ -537,7 +553,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 }
                 const uint64_t vd = vdesc + ((s * kTileBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kKSteps; ++kk) {
+                for (int kk = 0; kk < kPvSteps; ++kk) {
                     const uint64_t b = vd + ((kk * kKeysPerStep * 128) >> 4);
                     if constexpr (kFp8) mma_ts_f8(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, b, idPV, (acc || kk > 0));
                     else mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, b, idPV, (acc || kk > 0));
@@ -752,7 +768,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 const float f = grow ? fast_exp2(m - mx) : 1.f;   // 0 when m = -inf
                 if (grow) {
                     l *= f;
-                    if constexpr (kFp8 && kLse) lt *= f;
+                    if constexpr (kFp8 && (kLse || kPlo)) lt *= f;
                     m = mx;
                 }
                 const float off = bias - (m == -INFINITY ? 0.f : m);
@@ -762,6 +778,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 const uint64_t cc = f2_pack(csc, csc);
                 constexpr int kPk = kFp8 ? 32 : 64;   // packed words of P per row
                 uint32_t pk[kPk];
+                uint32_t pr[kPlo ? 32 : 1];           // kPlo: the residual term of P
                 if constexpr (!kFp8) {
                     const uint64_t oo = f2_pack(off, off);
                     // a mean tile's columns 64..127 (its lo terms, folded into 0..63)
@@ -803,8 +820,21 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                             const __nv_fp8x2_storage_t hi =
                                 __nv_cvt_float2_to_fp8x2(make_float2(p2, p3), __NV_SATFINITE, __NV_E4M3);
                             pk[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+                            if constexpr (kPlo) {
+                                const float2 d01 = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3)));
+                                const float2 d23 = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
+                                float r0, r1, r2, r3;
+                                f2_unpack(f2_add(f2_pack(p0, p1), f2_pack(-d01.x, -d01.y)), r0, r1);
+                                f2_unpack(f2_add(f2_pack(p2, p3), f2_pack(-d23.x, -d23.y)), r2, r3);
+                                const __nv_fp8x2_storage_t rl =
+                                    __nv_cvt_float2_to_fp8x2(make_float2(r0, r1), __NV_SATFINITE, __NV_E4M3);
+                                const __nv_fp8x2_storage_t rh =
+                                    __nv_cvt_float2_to_fp8x2(make_float2(r2, r3), __NV_SATFINITE, __NV_E4M3);
+                                pr[e] = (uint32_t)rl | ((uint32_t)rh << 16);
+                            }
                         }
                         tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+                        if constexpr (kPlo) tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(pr));
                         if constexpr (decltype(with_sum)::value) {
                             float t0, t1, t2, t3;
                             f2_unpack(ltp[0], t0, t1);
@@ -812,7 +842,9 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                             lt += (t0 + t1) + (t2 + t3);
                         }
                     };
-                    exps(std::integral_constant<bool, kLse>{});
+                    // kPlo: the denominator is the fp32 sum of the unrounded weights
+                    // (the two terms carry ~2^-8 relative), taken here
+                    exps(std::integral_constant<bool, kLse || kPlo>{});
                 }
                 if (any_grow && jl > 0) {
 #pragma unroll 1
@@ -842,6 +874,8 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     f2_unpack(acc2[0], r0, r1);
                     f2_unpack(acc2[1], r2, r3);
                     rs = (r0 + r1) + (r2 + r3);
+                } else if constexpr (kPlo) {
+                    rs = 0.f;                               // summed into lt with the exponentials
                 } else {
                     // decoded e4m3 weights summed in half2 (<= 128 * 256 < 65504)
                     __half2 hs[4];
@@ -876,7 +910,8 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             tc_fence_after();
             // O = (sum of weights * v codes) * v_scale / (sum of weights); for e4m3
             // both sums carry the factor 256, which cancels
-            const float inv = l > 0.f ? (kFp8 ? __ldg(a.v_scale + V.h) : 1.f) / l : 0.f;
+            const float den = kPlo ? lt : l;               // kPlo: the unrounded weights' sum
+            const float inv = den > 0.f ? (kFp8 ? __ldg(a.v_scale + V.h) : 1.f) / den : 0.f;
             const long long tok = rv.q_off + qv;
             const bool part = a.n_split > 1;            // split-KV: fp32 partial O of this part
             __nv_bfloat16 *dst = a.out + (tok * bd.h_q + hv) * kHeadDim;
@@ -908,9 +943,9 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             // the next unit's first PV MMA overwrites O only after this warp
             // group's next P handshake, which follows these reads
             tc_fence_before();
-            const float lsum = kFp8 && kLse ? lt : l;
+            const float lsum = kFp8 && (kLse || kPlo) ? lt : l;
             const float lse_v =
-                l > 0.f ? (m + __log2f(lsum) - (kFp8 ? 8.f : 0.f)) * 0.6931471805599453f : -INFINITY;
+                den > 0.f ? (m + __log2f(lsum) - (kFp8 ? 8.f : 0.f)) * 0.6931471805599453f : -INFINITY;
             if (valid && part) a.part_lse[((long long)V.split * bd.h_q + hv) * bd.total_q + tok] = lse_v;
             else if (valid && a.lse) a.lse[(long long)hv * bd.total_q + tok] = lse_v;
             ++kq;
@@ -1264,10 +1299,13 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     a.status = L.status;
     a.wait_ns = L.wait_ns;
     const bool want_lse = L.lse != nullptr || n_split > 1;
+    const bool plo = f8 && L.p_terms == 2;
     auto kern = L.v_dim_major
-                    ? (f8 ? (want_lse ? attn_kernel<true, true, true> : attn_kernel<true, false, true>)
+                    ? (f8 ? (plo ? (want_lse ? attn_kernel<true, true, true, true> : attn_kernel<true, false, true, true>)
+                                 : (want_lse ? attn_kernel<true, true, true> : attn_kernel<true, false, true>))
                           : attn_kernel<false, false, true>)
-                    : (f8 ? (want_lse ? attn_kernel<true, true, false> : attn_kernel<true, false, false>)
+                    : (f8 ? (plo ? (want_lse ? attn_kernel<true, true, false, true> : attn_kernel<true, false, false, true>)
+                                 : (want_lse ? attn_kernel<true, true, false> : attn_kernel<true, false, false>))
                           : attn_kernel<false, false, false>);
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttn)) != cudaSuccess)
         return fail("attention smem attribute", (int)e);

@@ -63,6 +63,7 @@ struct AttnLaunch {
     float *part_o;                    // [n_split, total_q, h_q, d] fp32 when n_split > 1
     float *part_lse;                  // [n_split, h_q, total_q] fp32 when n_split > 1
     bool v_dim_major;                 // value cache [num_pages, h_kv, d, page_size]
+    int p_terms;                      // e4m3: P in 1 term (e4m3 of 256 p) or 2 (plus the residual)
 };
 int launch_attn(const AttnLaunch &L, cudaStream_t st);
 // rows of the bf16 block-mean copies: at least one full 128-row TMA box

@@ -28,7 +28,7 @@ class FpParams(Structure):
     _fields_ = [("block", c_int), ("sink_tokens", c_int), ("local_tokens", c_int),
                 ("alpha", c_float), ("softmax_scale", c_float), ("mean_correction", c_int),
                 ("kv_splits", c_int), ("select_rule", c_int), ("top_k", c_int), ("top_p", c_float),
-                ("score_mode", c_int)]
+                ("score_mode", c_int), ("p_terms", c_int)]
 
 
 class FpProblem(Structure):

@@ -105,6 +105,11 @@ typedef struct {
     int top_k;            /* FP_SELECT_TOPK: blocks kept per row (>= 1) */
     float top_p;          /* FP_SELECT_TOPP: share of the row's score mass kept, (0, 1] */
     int score_mode;       /* fp_discover: FP_SCORE_PACKED or FP_SCORE_HEAD_UNION */
+    int p_terms;          /* FP_E4M3 attention only: the softmax weights P enter the PV
+                             product as 1 e4m3 term, e4m3(256 p) [V2 paper reading 4.2 (4)],
+                             or 2: that term plus the residual e4m3(256 p - term) in a second
+                             PV pass, which cuts the weights' rounding from 2^-4 to about
+                             2^-8 relative; 0 means 1 */
 } fp_params;
 
 /* Score modes of fp_discover.  PACKED is the reading of the V1 summary 3.1
@@ -164,7 +169,8 @@ typedef enum { FP_V_TOKEN_MAJOR = 0, FP_V_DIM_MAJOR = 1 } fp_v_layout;
 
 /* Defaults of the pages: B=128, sink 256, local 512, alpha 0.1, 1/sqrt(d),
  * mean correction on [V2 paper reading, section 4 configuration]; kv_splits 0
- * (chosen by the library); the threshold rule (top_k 0, top_p 0: unused). */
+ * (chosen by the library); the threshold rule (top_k 0, top_p 0: unused);
+ * p_terms 1 (the pages' e4m3 P). */
 fp_params fp_default_params(void);
 
 /* Sizes derived from the host descriptors (element counts, not bytes). */

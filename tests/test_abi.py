@@ -88,6 +88,16 @@ def test_default_params_are_the_pages_configuration(fp):
     p = fp.default_params()
     assert (p.block, p.sink_tokens, p.local_tokens, p.mean_correction) == (128, 256, 512, 1)
     assert abs(p.alpha - 0.1) < 1e-7 and p.softmax_scale == 0.0
+    assert p.p_terms == 1                       # the pages' single e4m3 term of P
+
+
+def test_p_terms_out_of_range_is_refused(fp):
+    pr, keep = problem(fp, [(300, 0), (256, 512)])
+    L = fp.lib()
+    for bad in (-1, 3):
+        prm = fp.default_params(p_terms=bad)
+        assert L.fp_num_rows(ctypes.byref(pr), ctypes.byref(prm)) == -1
+        assert L.fp_attn_workspace_size(ctypes.byref(pr), ctypes.byref(prm)) == 0
 
 
 @pytest.mark.parametrize("mutate,code", [

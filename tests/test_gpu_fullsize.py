@@ -51,7 +51,7 @@ def sample_rows(spec, case, r, score_h, offs, rng, n_random, n_near=8, alpha=0.1
 
 
 def sampled_parity(spec, alpha=0.1, mean_corr=(True,), rows_per_request=32, queries_per_row=64,
-                   max_abs=BF16_MAX_ABS, mean_abs=BF16_MEAN_ABS, lse_abs=2e-2, seed=0):
+                   max_abs=BF16_MAX_ABS, mean_abs=BF16_MEAN_ABS, lse_abs=2e-2, seed=0, p_terms=1):
     """The three calls of the benchmark step on the full workload, then, on
     sampled rows: pooled means of every block, score rows, their index rows
     (exact outside the flagged band) and sampled output rows of the
@@ -61,7 +61,7 @@ def sampled_parity(spec, alpha=0.1, mean_corr=(True,), rows_per_request=32, quer
     import oracle
     from block_sparse_long_fp_gb300 import fprefill
     case = synth.make_case(spec)
-    prm = fprefill.default_params(alpha=alpha)
+    prm = fprefill.default_params(alpha=alpha, p_terms=p_terms)
     layer = fprefill.layer_from_case(case, params=prm)
     # one pass of the path, the three calls of the benchmark step
     k_mean, v_mean, score = layer.discover()
@@ -154,6 +154,12 @@ def test_qwen30b_128k_bf16_sparse_regime():
 
 def test_qwen30b_128k_e4m3():
     sampled_parity(synth.config_spec(3, dtype="e4m3"), max_abs=FP8_MAX_ABS, mean_abs=6e-3, lse_abs=FP8_LSE_ABS)
+
+
+def test_qwen30b_128k_e4m3_two_term_p():
+    """The 128K e4m3 layer with queries x 16 and P in two e4m3 terms."""
+    sampled_parity(synth.config_spec(3, dtype="e4m3", logit_scale=16.0), max_abs=FP8_MAX_ABS, mean_abs=6e-3,
+                   lse_abs=FP8_LSE_ABS, rows_per_request=16, p_terms=2)
 
 
 def test_qwen30b_128k_e4m3_sparse_regime():
