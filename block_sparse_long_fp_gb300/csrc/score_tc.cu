@@ -55,7 +55,7 @@ struct ScoreCfg {
     static constexpr int kTmemBufs = 2 * kBufs;
     static constexpr int kSmStage = 0;
     static constexpr int kSmCtl = kSmStage + kStages * kStageBytes;
-    static constexpr int kSmAcc = kSmCtl + 512;                // per-warp column sums [8][max_nkb]
+    static constexpr int kSmAcc = kSmCtl + 512;                // column sums [8 or 2][max_nkb]
     // TMEM: the S buffers (kBufs per head slot), then the query tiles as MMA
     // A operands (128 rows x 128 bf16 = 64 columns each), two buffers of two
     // head slots, so the next pair's queries go in while this pair runs
@@ -66,7 +66,10 @@ struct ScoreCfg {
     static constexpr int B_TE = B_TF + 4, B_DR = B_TE + 4, B_N = B_DR + 1;   // B_DR: the MMAs' drain
     static_assert(kTmemQ + 256 <= 512, "TMEM budget");
     static_assert(B_N * 8 + 128 <= 512, "control block");
-    static size_t smem_bytes(int max_nkb) { return (size_t)kSmAcc + 8 * sizeof(float) * max_nkb + 1024; }
+    // shared: one column-sum array per head slot instead of one per row warp
+    static size_t smem_bytes(int max_nkb, bool shared = false) {
+        return (size_t)kSmAcc + (shared ? 2 : 8) * sizeof(float) * max_nkb + 1024;
+    }
 };
 
 struct ScoreTcArgs {
@@ -159,7 +162,11 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
 // kFp8: the query tiles are e4m3 codes; each row warpgroup loads its rows,
 // converts them exactly to bf16 and writes the swizzled tile itself (the
 // mean terms are bf16 either way), and the head's scale joins the exponent.
-template <bool kFp8, int kCh>
+// kShared: the four warps of a head slot add their column sums into one array
+// (shared-memory atomics, so the order of the additions varies from run to
+// run) instead of one array each: rows past 1024 blocks then still fit with
+// 128-block chunks.  Without it every sum is added in a fixed order.
+template <bool kFp8, int kCh, bool kShared>
 __global__ void __launch_bounds__(kScThreads, 1)
 score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmM, const ScoreTcArgs a) {
@@ -293,12 +300,18 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
         const int rowt = quarter * 32 + lane;
         const bool row_valid = il * kBlock + rowt < rq.lq;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        float *my_acc = acc + (w * 4 + quarter) * a.acc_stride;   // this warp's 32 rows, summed
-        for (int J = lane; J < ncol; J += 32) my_acc[J] = 0.f;
-        __syncwarp();
-        int u = 0;
-        bool ok = true;
+        // this warp's 32 rows, summed (kShared: the head slot's 128 rows)
+        float *my_acc = acc + (kShared ? w : w * 4 + quarter) * a.acc_stride;
         unsigned gen = 0;
+        bool ok = true;
+        if constexpr (kShared) {
+            for (int J = quarter * 32 + lane; J < ncol; J += 128) my_acc[J] = 0.f;
+            ok = rows_sync(sync_ctr, gen, lane, abort_flag, a.status, a.wait_ns);   // cleared before any add
+        } else {
+            for (int J = lane; J < ncol; J += 32) my_acc[J] = 0.f;
+            __syncwarp();
+        }
+        int u = 0;
         // head hq's query rows -> query buffer qb in TMEM as the MMA's A operand
         // (e4m3 codes are converted exactly to bf16); 32 columns = 64 values at
         // a time.  Returns false if the CTA is aborting.
@@ -422,7 +435,10 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                             }
                             // lane L now gets the sum of column J0 + L over this warp's 32 rows
                             const float s0 = transpose_reduce32(v0, lane);
-                            if (J0 + lane < ncol) my_acc[J0 + lane] += s0;
+                            if (J0 + lane < ncol) {
+                                if constexpr (kShared) atomicAdd(my_acc + J0 + lane, s0);
+                                else my_acc[J0 + lane] += s0;
+                            }
                         }
                     }
                 }
@@ -435,6 +451,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                 const int t = threadIdx.x - 128;
                 const int st = a.acc_stride;
                 auto head_sum = [&](int ww, int J) {
+                    if constexpr (kShared) return acc[ww * st + J];
                     const float *b0 = acc + ww * 4 * st;
                     return (b0[J] + b0[st + J]) + (b0[2 * st + J] + b0[3 * st + J]);
                 };
@@ -474,7 +491,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                     if (pr > 0) u = fmaxf(u, out[J]);
                     out[J] = u;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) acc[k * st + J] = 0.f;
+                    for (int k = 0; k < (kShared ? 2 : 8); ++k) acc[k * st + J] = 0.f;
                 }
                 ok = rows_sync(sync_ctr, gen, lane, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
@@ -487,6 +504,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
             const int t = threadIdx.x - 128;
             const int st = a.acc_stride;
             auto colsum = [&](int J) {
+                if constexpr (kShared) return acc[J] + acc[st + J];
                 return ((acc[J] + acc[st + J]) + (acc[2 * st + J] + acc[3 * st + J])) +
                        ((acc[4 * st + J] + acc[5 * st + J]) + (acc[6 * st + J] + acc[7 * st + J]));
             };
@@ -590,11 +608,11 @@ bool map3(CUtensorMap *m, const void *base, long long n1, long long n2, long lon
 // rows of each mean term: at least one box of the widest chunk
 int score_tc_rows_pad(const BatchDesc &bd) { return bd.total_kb > 128 ? bd.total_kb : 128; }
 
-// shared memory of the build that serves rows of up to max_nkb blocks
-size_t score_tc_smem_bytes(int max_nkb) {
-    const size_t wide = ScoreCfg<128>::smem_bytes(max_nkb);
-    return wide <= 227 * 1024 ? wide : ScoreCfg<64>::smem_bytes(max_nkb);
-}
+// the build that serves rows of up to max_nkb blocks: 128-block chunks, with a
+// column-sum array per row warp (fixed summation order) while it fits, then
+// one per head slot
+static bool score_tc_shared(int max_nkb) { return ScoreCfg<128>::smem_bytes(max_nkb) > 227 * 1024; }
+size_t score_tc_smem_bytes(int max_nkb) { return ScoreCfg<128>::smem_bytes(max_nkb, score_tc_shared(max_nkb)); }
 
 cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
                             long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
@@ -608,8 +626,8 @@ cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long l
     if (e != cudaSuccess) return e;
     CUtensorMap tmQ, tmM;
     (void)q_stride_head;
-    const bool wide = ScoreCfg<128>::smem_bytes(bd.max_nkb) <= 227 * 1024;
-    if (!map3(&tmM, terms, bd.h_kv, 3LL * rows_pad, kHeadDim, (long long)bd.h_kv * kHeadDim, wide ? 128 : 64))
+    const bool shared = score_tc_shared(bd.max_nkb);
+    if (!map3(&tmM, terms, bd.h_kv, 3LL * rows_pad, kHeadDim, (long long)bd.h_kv * kHeadDim, 128))
         return cudaErrorInvalidValue;
     ScoreTcArgs a;
     a.score = score;
@@ -631,8 +649,8 @@ cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long l
     a.wait_ns = wait_ns;
     tmQ = tmM;                           // not read: the row warps load the queries themselves
     const int smem = (int)score_tc_smem_bytes(bd.max_nkb);
-    auto kern = wide ? (fp8 ? score_tc_kernel<true, 128> : score_tc_kernel<false, 128>)
-                     : (fp8 ? score_tc_kernel<true, 64> : score_tc_kernel<false, 64>);
+    auto kern = shared ? (fp8 ? score_tc_kernel<true, 128, true> : score_tc_kernel<false, 128, true>)
+                       : (fp8 ? score_tc_kernel<true, 128, false> : score_tc_kernel<false, 128, false>);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<bd.total_rows, kScThreads, smem, st>>>(bd, tmQ, tmM, a);
