@@ -181,15 +181,22 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             const __grid_constant__ CUtensorMap tmKm, const __grid_constant__ CUtensorMap tmVm,
             const AttnArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned (128-byte swizzle atoms).  smem, the barriers and the
+    // abort flag are derived from smem_raw by offsets (not through an integer
+    // round trip of a generic pointer), so every role addresses them in the
+    // shared window: no 64-bit pointer stays live, and the kernel spills
+    // nothing (with one it reloaded at every wait site, and extra code in the
+    // MMA thread put a local load beside each MMA)
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmemCtl);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kSmemMisc);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kSmemMisc + 4);
+    const uint32_t abort_flag = smem_u32(smem) + kSmemMisc + 4;   // shared-window address
     UnitMeta *meta = reinterpret_cast<UnitMeta *>(smem + kSmemMeta);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t sbase = smem_u32(smem);
-    auto bar = [&](int k) { return smem_u32(&bars[k]); };
+    const uint32_t bars_a = smem_u32(bars);
+    auto bar = [&](int k) { return bars_a + 8u * (uint32_t)k; };
     // a 128 x 128 tile is 32 KB of bf16 in two 64-column boxes, or 16 KB of
     // e4m3 in one 128-column box; smem slots are 32 KB either way
     constexpr int kT = kFp8 ? kTileBytes / 2 : kTileBytes;
@@ -206,7 +213,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             if (k == BAR_ME || k == BAR_ME + 1) cnt = kMetaConsumers;
             mbar_init(bar(k), cnt);
         }
-        *abort_flag = 0;
+        st_shared_volatile(abort_flag, 0);
         fence_barrier_init();
         fence_proxy_async();
     }
@@ -492,7 +499,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             }
             // after an abort, the copies armed last land before the CTA leaves
             // (otherwise every copy has been consumed already)
-            if (lane == 0 && *abort_flag) {
+            if (lane == 0 && ld_shared_volatile(abort_flag)) {
                 if (q_ph >= 0) mbar_wait_drain(bar(BAR_Q), q_ph);
                 // items before `it` were armed in full, except the one whose slot
                 // wait gave up: its K only when the V wait was the one that gave up
@@ -552,8 +559,11 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     return;
                 }
                 const uint64_t vd = vdesc + ((s * kTileBytes) >> 4);
+                // a bf16 mean tile's P is zero past column 64: half the steps
+                const int nsteps = (!kFp8 && !kept) ? kPvSteps / 2 : kPvSteps;
 #pragma unroll
                 for (int kk = 0; kk < kPvSteps; ++kk) {
+                    if (kk >= nsteps) break;
                     const uint64_t b = vd + ((kk * kKeysPerStep * 128) >> 4);
                     if constexpr (kFp8) mma_ts_f8(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, b, idPV, (acc || kk > 0));
                     else mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, b, idPV, (acc || kk > 0));
@@ -620,7 +630,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 if (!good) break;
                 ++kq;
             }
-            if (*abort_flag) {                         // after an abort, every MMA issued is done
+            if (ld_shared_volatile(abort_flag)) {          // after an abort, every MMA issued is done
                 tc_commit(bar(BAR_DR));                // before the CTA leaves
                 mbar_wait_drain(bar(BAR_DR), 0);
             }

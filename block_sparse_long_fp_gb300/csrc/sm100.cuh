@@ -66,6 +66,36 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+__device__ __forceinline__ int ld_shared_volatile(uint32_t a) {
+    int v;
+    asm volatile("ld.volatile.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_volatile(uint32_t a, int v) {
+    asm volatile("st.volatile.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+// The same wait with the abort flag given by its shared-window address.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t abort_flag, int *status,
+                                          uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (ld_shared_volatile(abort_flag)) return false;
+            if (status && *reinterpret_cast<volatile int *>(status) == FP_ERR_TIMEOUT) {
+                st_shared_volatile(abort_flag, 1);
+                return false;
+            }
+            if (global_ns() - t0 > limit_ns) {
+                set_status(status, FP_ERR_TIMEOUT);
+                st_shared_volatile(abort_flag, 1);
+                return false;
+            }
+        }
+    }
+}
+
 // Wait for a phase that work already in flight will complete (TMA copies or
 // MMAs issued before the CTA stopped), so that a CTA leaving after an abort
 // does not leave copies landing in its shared memory or MMAs writing its
