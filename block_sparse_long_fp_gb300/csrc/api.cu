@@ -104,8 +104,8 @@ float softmax_scale_of(const fp_params *prm, int d) {
 
 int *status_ptr(void *ws) { return reinterpret_cast<int *>(ws); }
 
-// Scores run on the tensor cores while the per-warp column sums fit in shared
-// memory (rows up to 2048 key blocks); longer rows use the fp32 CUDA-core kernel.
+// Scores run on the tensor cores while the column sums fit in shared memory
+// (rows up to 12480 key blocks); longer rows use the fp32 CUDA-core kernel.
 bool use_score_tc(const fp_problem *p, const BatchDesc &bd) {
     (void)p;
     return score_tc_smem_bytes(bd.max_nkb) <= 227 * 1024;
@@ -244,7 +244,7 @@ fp_status fp_discover(const fp_problem *p, const fp_params *prm, float *k_mean, 
         else
             e = launch_score_tc(bd, fp8, p->q, p->q_stride_tok, p->q_stride_head, p->q_scale, k_mean,
                                 softmax_scale_of(prm, p->d), score,
-                                reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + kWsHeaderBytes),
+                                static_cast<char *>(ws) + kWsHeaderBytes,
                                 status_ptr(ws), g_wait_ns, st, nullptr, head_union);
         if (e != cudaSuccess) return FP_ERR_CUDA;
     }
@@ -319,7 +319,7 @@ fp_status fp_discover_select(const fp_problem *p, const fp_params *prm, float *k
                    ? FP_OK
                    : FP_ERR_CUDA;
     }
-    __nv_bfloat16 *terms = reinterpret_cast<__nv_bfloat16 *>(w + kWsHeaderBytes);
+    void *terms = w + kWsHeaderBytes;
     const float scale = softmax_scale_of(prm, p->d);
     cudaError_t e;
     if (tc && prm->select_rule == FP_SELECT_THRESHOLD && !head_union) {

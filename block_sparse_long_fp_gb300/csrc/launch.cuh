@@ -18,12 +18,16 @@ cudaError_t launch_select(const BatchDesc &bd, float alpha, int sink_blocks, int
                           unsigned long long wait_ns, cudaStream_t st);
 inline size_t select_state_bytes(const BatchDesc &bd) { return (size_t)((bd.total_rows + 7) / 8 + 1) * 8; }
 size_t score_smem_bytes(int max_nkb);
-// tensor-core score map (bf16 inputs): the three bf16 terms of the means live in
-// a workspace of score_tc_terms_bytes()
+// tensor-core score map: the two fp16 terms of the key means, then the scale
+// exponent of each (128-block chunk, kv head), live in a workspace of
+// score_tc_terms_bytes()
 int score_tc_rows_pad(const BatchDesc &bd);
 size_t score_tc_smem_bytes(int max_nkb);   // the tensor-core path needs this <= 227 KB
+inline size_t score_tc_kexp_offset(const BatchDesc &bd) {
+    return ((size_t)2 * score_tc_rows_pad(bd) * bd.h_kv * kHeadDim * 2 + 255) / 256 * 256;
+}
 inline size_t score_tc_terms_bytes(const BatchDesc &bd) {
-    return (size_t)3 * score_tc_rows_pad(bd) * bd.h_kv * kHeadDim * 2;
+    return score_tc_kexp_offset(bd) + (size_t)(bd.total_kb > 0 ? bd.total_kb : 1) * bd.h_kv;
 }
 // fused selection at the end of the tensor-core score kernel (threshold rule)
 struct ScoreSelect {
@@ -34,7 +38,7 @@ struct ScoreSelect {
 };
 cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
                             long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
-                            float *score, __nv_bfloat16 *terms, int *status, unsigned long long wait_ns,
+                            float *score, void *terms_ws, int *status, unsigned long long wait_ns,
                             cudaStream_t st, const ScoreSelect *sel = nullptr, bool head_union = false);
 cudaError_t launch_select_gather(const BatchDesc &bd, const int *keep_pad, const int *counts, int *row_ptr,
                                  int *col_idx, long long col_capacity, int *nnz, int *status, cudaStream_t st);

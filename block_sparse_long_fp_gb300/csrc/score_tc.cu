@@ -4,19 +4,27 @@
 // row: logits against the pooled keys, normalised by the row's own maximum,
 // exponentiated and summed over the query block; then each score row divided
 // by its largest entry) decide, through a threshold, which blocks are kept.
-// Decisions must not move relative to the float64 definition, so the pooled
-// keys enter the MMA as three bf16 terms, kmean = hi + mid + lo (24
-// significant bits, like fp32); Q is exactly representable in bf16, and so are
-// e4m3 query codes, which the row warps convert.
+// Decisions must not move relative to the float64 definition (a block's score
+// may move by far less than 1e-4 of the threshold), so the MMAs run on fp16
+// operands near fp32 accuracy:
+//  * the pooled keys of each chunk of 128 blocks and kv head are scaled by a
+//    power of two 2^e (their largest magnitude lands in [2^14, 2^15)) and
+//    enter as two fp16 terms, kmean * 2^e = hi + lo (22 significant bits);
+//  * each query row is scaled by its own power of two 2^f the same way; bf16
+//    values (8 significant bits) and e4m3 codes are exact in fp16 then;
+//  * products of fp16 values are exact in the fp32 accumulator, and scaling
+//    by powers of two commutes with its rounding, so 2^-(e+f) joins the
+//    exponent's fp32 constant and the logits are those of the unscaled
+//    operands.
 //
 // One CTA per score row (request, query block I, kv head h).  The g query
 // heads of the group go in pairs (A, B), each head a 128-query tile (M = 128):
-//   pass 0: S = Q Kmean^T over the row's key blocks 0..I, 64 at a time -> row max
+//   pass 0: S = Q Kmean^T over the row's key blocks 0..I, 128 at a time -> row max
 //   pass 1: the same S again -> exp2((s - max) * scale * log2 e), summed down
 //           the 128 queries (a transpose-reduce across each warp's 32 rows)
 //           into per-warp column sums in shared memory;
 // then S' = the sum of all warps' column sums (fixed order) and the row is
-// divided by its maximum.  Warp 0 issues TMA loads (the three mean terms of a
+// divided by its maximum.  Warp 0 issues TMA loads (the two mean terms of a
 // chunk of key blocks, shared by both heads, in a ring of stages), warp 1
 // issues the MMAs, warpgroup A (warps 4-7) and warpgroup B (warps 8-11) each
 // own one head of the pair and its TMEM S buffers, one query row per thread,
@@ -41,23 +49,22 @@ namespace {
 
 constexpr int kScThreads = 384;
 
-// Layout of one build of the kernel for a chunk of kChunk key blocks (MMA N):
-// 128-block chunks halve the MMA instructions per FLOP (measured 2.9 vs 4.0
-// ms at 128K) but leave room for per-warp column sums of rows up to 1024
-// blocks only; 64-block chunks take rows up to 2048 blocks.
+// Layout of one build of the kernel for a chunk of kChunk key blocks (MMA N;
+// also the span of one scale of the key means).
 template <int C>
 struct ScoreCfg {
     static constexpr int kChunk = C;
+    static constexpr int kTerms = 2;                           // fp16 terms of the key means
     static constexpr int kBufs = C == 64 ? 2 : 1;              // TMEM S buffers per head slot
     static constexpr int kTermBytes = C * kHeadDim * 2;        // one term of one chunk
-    static constexpr int kStageBytes = 3 * kTermBytes;
+    static constexpr int kStageBytes = kTerms * kTermBytes;
     static constexpr int kStages = C == 64 ? 3 : 2;
     static constexpr int kTmemBufs = 2 * kBufs;
     static constexpr int kSmStage = 0;
     static constexpr int kSmCtl = kSmStage + kStages * kStageBytes;
     static constexpr int kSmAcc = kSmCtl + 512;                // column sums [8 or 2][max_nkb]
     // TMEM: the S buffers (kBufs per head slot), then the query tiles as MMA
-    // A operands (128 rows x 128 bf16 = 64 columns each), two buffers of two
+    // A operands (128 rows x 128 fp16 = 64 columns each), two buffers of two
     // head slots, so the next pair's queries go in while this pair runs
     static constexpr int kTmemQ = kTmemBufs * C;
     // barriers: Q full/empty per (buffer, head slot), stage full/empty, TMEM
@@ -75,11 +82,12 @@ struct ScoreCfg {
 struct ScoreTcArgs {
     float *score;
     float scale_log2;
+    const int8_t *kexp;       // e of each (chunk, kv head): at [chunk's first block][h]
     const uint8_t *q8;        // e4m3 queries (codes); strides in elements
     const __nv_bfloat16 *q16; // bf16 queries
     long long q_stride_tok, q_stride_head;
     const float *q_scale;     // e4m3 only: per query head
-    int rows_pad;             // rows of each mean term in the split array
+    int rows_pad;             // rows of each mean term in the term array
     int acc_stride;           // floats per warp accumulator (>= the row length)
     // fused selection (null: scores only): each row's kept blocks, ascending,
     // into keep_pad at the row's score-map offset, and their count
@@ -97,7 +105,7 @@ struct ScoreTcArgs {
 // adds one arrival to a shared counter and spins (bounded, like the mbarrier
 // waits) until all eight warps of this generation have arrived.  Returns false
 // if the CTA is aborting.
-__device__ __forceinline__ bool rows_sync(unsigned *ctr, unsigned &gen, int lane, volatile int *abort_flag,
+__device__ __forceinline__ bool rows_sync(unsigned *ctr, unsigned &gen, int lane, uint32_t abort_flag,
                                           int *status, unsigned long long wait_ns) {
     gen += 8;
     bool ok = true;
@@ -109,10 +117,10 @@ __device__ __forceinline__ bool rows_sync(unsigned *ctr, unsigned &gen, int lane
         const uint64_t t0 = global_ns();
         for (uint32_t it = 0; *vc < gen; ++it) {
             if ((it & 63u) == 63u) {
-                if (*abort_flag) { ok = false; break; }
+                if (ld_shared_volatile(abort_flag)) { ok = false; break; }
                 if (global_ns() - t0 > wait_ns) {
                     set_status(status, FP_ERR_TIMEOUT);
-                    *abort_flag = 1;
+                    st_shared_volatile(abort_flag, 1);
                     ok = false;
                     break;
                 }
@@ -125,9 +133,23 @@ __device__ __forceinline__ bool rows_sync(unsigned *ctr, unsigned &gen, int lane
     return ok;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+    __half2 v = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// 2^e as a float, for |e| <= 126
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// The power-of-two exponent that brings a largest magnitude (its fp32 bit
+// pattern) into [2^14, 2^15): under fp16's largest finite value, with 2^29
+// of range below it.  0 for a zero (or subnormal) maximum; clamped so that
+// 2^e and 2^-e stay normal floats.
+__host__ __device__ __forceinline__ int fp16_scale_exp(uint32_t max_bits) {
+    const int E = (int)((max_bits >> 23) & 0xffu);
+    if (E == 0) return 0;
+    const int e = 141 - E;
+    return e < -100 ? -100 : (e > 100 ? 100 : e);
 }
 
 // Column sums of a 32x32 block held one row per lane (v[c] = column c of
@@ -159,36 +181,41 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
     return keep + __shfl_xor_sync(0xffffffffu, send, 1);
 }
 
-// kFp8: the query tiles are e4m3 codes; each row warpgroup loads its rows,
-// converts them exactly to bf16 and writes the swizzled tile itself (the
-// mean terms are bf16 either way), and the head's scale joins the exponent.
+// kFp8: the query tiles are e4m3 codes, converted exactly to fp16 (no row
+// scale), and the head's scale joins the exponent.  bf16 queries get a row
+// scale.
 // kShared: the four warps of a head slot add their column sums into one array
 // (shared-memory atomics, so the order of the additions varies from run to
-// run) instead of one array each: rows past 1024 blocks then still fit with
-// 128-block chunks.  Without it every sum is added in a fixed order.
+// run) instead of one array each: rows past 3120 blocks (up to 12480) then
+// still fit.  Without it every sum is added in a fixed order.
 template <bool kFp8, int kCh, bool kShared>
 __global__ void __launch_bounds__(kScThreads, 1)
 score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmM, const ScoreTcArgs a) {
     using Cfg = ScoreCfg<kCh>;
+    static_assert(kCh == 128, "the key means' scales span 128-block chunks");
     constexpr int kChunk = Cfg::kChunk, kBufs = Cfg::kBufs, kTermBytes = Cfg::kTermBytes;
     constexpr int kStageBytes = Cfg::kStageBytes, kStages = Cfg::kStages, kSmStage = Cfg::kSmStage;
     constexpr int kSmCtl = Cfg::kSmCtl, kSmAcc = Cfg::kSmAcc, kTmemQ = Cfg::kTmemQ;
     constexpr int B_QF = Cfg::B_QF, B_QE = Cfg::B_QE, B_SF = Cfg::B_SF, B_SE = Cfg::B_SE;
     constexpr int B_TF = Cfg::B_TF, B_TE = Cfg::B_TE, B_DR = Cfg::B_DR, B_N = Cfg::B_N;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned; derived from smem_raw by an offset, and the barriers
+    // and the abort flag addressed in the shared window (no generic pointer
+    // kept live)
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float *acc = reinterpret_cast<float *>(smem + kSmAcc);              // [4 warps][acc_stride]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmCtl);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kSmCtl + B_N * 8);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kSmCtl + B_N * 8 + 4);
+    const uint32_t abort_flag = smem_u32(smem) + kSmCtl + B_N * 8 + 4;
     float *red = reinterpret_cast<float *>(smem + kSmCtl + B_N * 8 + 16);   // [8]
     unsigned *sync_ctr = reinterpret_cast<unsigned *>(smem + kSmCtl + B_N * 8 + 48);
     float *red_h = reinterpret_cast<float *>(smem + kSmCtl + B_N * 8 + 64);    // [16]
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t sbase = smem_u32(smem);
-    auto bar = [&](int k) { return smem_u32(&bars[k]); };
+    const uint32_t bars_a = smem_u32(bars);
+    auto bar = [&](int k) { return bars_a + 8u * (uint32_t)k; };
 
     const int row = bd.total_rows - 1 - blockIdx.x;           // heavy (late) rows first
     const int r = req_of_row(bd, row);
@@ -209,7 +236,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
     if (threadIdx.x == 0) {
         for (int k = 0; k < B_N; ++k)
             mbar_init(bar(k), ((k >= B_TE && k < B_TE + 4) || (k >= B_QF && k < B_QF + 4)) ? 128u : 1u);
-        *abort_flag = 0;
+        st_shared_volatile(abort_flag, 0);
         *sync_ctr = 0u;
         fence_barrier_init();
         fence_proxy_async();
@@ -228,7 +255,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
             // ================= TMA producer =================
             tma_prefetch_desc(&tmM);
             int step = 0;
-            for (int pr = 0; pr < npairs && !*abort_flag; ++pr) {
+            for (int pr = 0; pr < npairs && !ld_shared_volatile(abort_flag); ++pr) {
                 for (int k = 0; k < steps_per_pair; ++k, ++step) {
                     const int c = k % nch;
                     const int s = step % kStages, use = step / kStages;
@@ -236,7 +263,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                         goto producer_done;
                     mbar_expect_tx(bar(B_SF + s), kStageBytes);
                     const uint32_t dst = sbase + kSmStage + s * kStageBytes;
-                    for (int t = 0; t < 3; ++t)
+                    for (int t = 0; t < Cfg::kTerms; ++t)
                         for (int hf = 0; hf < 2; ++hf)
                             tma_load_3d(dst + t * kTermBytes + hf * (kTermBytes / 2), &tmM, bar(B_SF + s), hf * 64, h,
                                         t * a.rows_pad + rq.kb_base + c * kChunk);
@@ -245,12 +272,12 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
         producer_done:
             // after an abort, the copies of the last stages armed land before the
             // CTA leaves (otherwise the MMAs have consumed every stage already)
-            if (*abort_flag)
+            if (ld_shared_volatile(abort_flag))
                 for (int j = step > kStages ? step - kStages : 0; j < step; ++j)
                     mbar_wait_drain(bar(B_SF + j % kStages), (j / kStages) & 1);
         } else if (warp == 1 && lane == 0) {
             // ================= MMA issuer =================
-            constexpr uint32_t idS = idesc_bf16(128, kChunk, false);
+            constexpr uint32_t idS = idesc_f16(128, kChunk, false);
             int step = 0;
             int uses[2] = {0, 0};                  // TMEM-buffer uses per head slot
             for (int pr = 0; pr < npairs; ++pr) {
@@ -275,7 +302,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                         const uint32_t dt = tmem + (kBufs * w + b) * kChunk;
                         const uint32_t qt = tmem + kTmemQ + (2 * qb + w) * 64;   // A: 16 d-values per 8 columns
 #pragma unroll
-                        for (int t = 0; t < 3; ++t)
+                        for (int t = 0; t < Cfg::kTerms; ++t)
 #pragma unroll
                             for (int kk = 0; kk < kHeadDim / 16; ++kk) {
                                 const uint32_t boff = t * kTermBytes + (kk >> 2) * (kTermBytes / 2) + (kk & 3) * 32;
@@ -288,7 +315,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                 for (int w = 0; w < nw; ++w) tc_commit(bar(B_QE + 2 * qb + w));
             }
         mma_done:
-            if (*abort_flag) {                      // after an abort, every MMA issued is done
+            if (ld_shared_volatile(abort_flag)) {   // after an abort, every MMA issued is done
                 tc_commit(bar(B_DR));               // before the CTA leaves
                 mbar_wait_drain(bar(B_DR), 0);
             }
@@ -312,10 +339,11 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
             __syncwarp();
         }
         int u = 0;
-        // head hq's query rows -> query buffer qb in TMEM as the MMA's A operand
-        // (e4m3 codes are converted exactly to bf16); 32 columns = 64 values at
-        // a time.  Returns false if the CTA is aborting.
-        auto put_queries = [&](int pr_q) -> bool {
+        // head hq's query rows -> query buffer qb in TMEM as the MMA's A operand,
+        // in fp16: e4m3 codes exactly as they are; bf16 rows scaled by 2^f_out
+        // (exact: 8 significant bits within fp16's range).  Returns false if
+        // the CTA is aborting.
+        auto put_queries = [&](int pr_q, int &f_out) -> bool {
             const int qb = pr_q & 1;
             if (pr_q >= 2) {                       // the buffer's previous pair is done with it
                 const bool got = mbar_wait(bar(B_QE + 2 * qb + w), ((pr_q >> 1) & 1) ^ 1, abort_flag, a.status,
@@ -324,17 +352,35 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
             }
             const int hq = h * g + 2 * pr_q + w;
             const long long el = (long long)(rq.q_off + il * kBlock + rowt) * a.q_stride_tok + (long long)hq * a.q_stride_head;
+            const uint32_t qdst = lane_base + kTmemQ + (2 * qb + w) * 64;
+            if constexpr (!kFp8) {
+                uint32_t qw[64];
+                const uint4 *src = reinterpret_cast<const uint4 *>(a.q16 + el);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t qw[32];
-                if constexpr (!kFp8) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(a.q16 + el) + half * 8;
+                for (int v = 0; v < 16; ++v) {
+                    const uint4 c = row_valid ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                    qw[4 * v] = c.x; qw[4 * v + 1] = c.y; qw[4 * v + 2] = c.z; qw[4 * v + 3] = c.w;
+                }
+                // the row's largest magnitude: bf16 bit patterns without the sign
+                // order like their values
+                uint32_t mx2 = 0u;
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const uint4 c = row_valid ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-                        qw[4 * v] = c.x; qw[4 * v + 1] = c.y; qw[4 * v + 2] = c.z; qw[4 * v + 3] = c.w;
-                    }
-                } else {
+                for (int k = 0; k < 64; ++k) mx2 = __vmaxu2(mx2, qw[k] & 0x7fff7fffu);
+                const uint32_t mx16 = (mx2 >> 16) > (mx2 & 0xffffu) ? (mx2 >> 16) : (mx2 & 0xffffu);
+                const int f = fp16_scale_exp(mx16 << 16);
+                const float sf = pow2f(f);
+#pragma unroll
+                for (int k = 0; k < 64; ++k) {
+                    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qw[k]));
+                    qw[k] = pack_f16x2(x.x * sf, x.y * sf);
+                }
+                tmem_st32(qdst, *reinterpret_cast<const uint32_t(*)[32]>(qw));
+                tmem_st32(qdst + 32, *reinterpret_cast<const uint32_t(*)[32]>(qw + 32));
+                f_out = f;
+            } else {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t qw[32];
                     const uint4 *src = reinterpret_cast<const uint4 *>(a.q8 + el) + half * 4;
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
@@ -343,12 +389,13 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
                             const __nv_fp8x2_storage_t c2v = (__nv_fp8x2_storage_t)(cw[k / 2] >> (16 * (k & 1)));
-                            const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(c2v, __NV_E4M3)));
-                            qw[8 * v + k] = pack_bf16x2(f.x, f.y);
+                            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(c2v, __NV_E4M3);
+                            qw[8 * v + k] = (uint32_t)hr.x | ((uint32_t)hr.y << 16);
                         }
                     }
+                    tmem_st32(qdst + half * 32, qw);
                 }
-                tmem_st32(lane_base + kTmemQ + (2 * qb + w) * 64 + half * 32, qw);
+                f_out = 0;
             }
             tmem_st_wait();
             tc_fence_before();
@@ -365,8 +412,10 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
             asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
             if constexpr (!kFp8) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + 128));
         };
-        if (w < g) ok = put_queries(0);
+        int fq = 0, fq_next = 0;                          // row scale exponents (this pair, the next)
+        if (w < g) ok = put_queries(0, fq);
         for (int pr = 0; pr < npairs && ok; ++pr) {
+            if (pr > 0) fq = fq_next;
             // a slot without a head in this pair (odd g, last pair) has no passes;
             // under the union of heads it still takes part in the pair's syncs
             const bool has_head = 2 * pr + w < g;
@@ -375,17 +424,20 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
             const bool next = 2 * (pr + 1) + w < g;       // this slot has a head in the next pair
             if (next) prefetch_queries(pr + 1);
             const float c2 = kFp8 ? a.scale_log2 * __ldg(a.q_scale + hq) : a.scale_log2;
-            float m = -INFINITY;
+            const float c2q = c2 * pow2f(-fq);          // undoes the row's query scale
+            float m = -INFINITY;                        // the row's largest logit (unscaled)
             float mc2 = 0.f;
             for (int pass = 0; pass < 2 && ok && has_head; ++pass) {
                 if (pass == 1) {
                     mc2 = !row_valid ? INFINITY : (m == -INFINITY ? 0.f : m * c2);
                     // the next pair's queries go into the other buffer while this
                     // pair's second pass keeps the tensor cores busy
-                    if (next && !put_queries(pr + 1)) { ok = false; break; }
+                    if (next && !put_queries(pr + 1, fq_next)) { ok = false; break; }
                 }
                 for (int c = 0; c < nch; ++c, ++u) {
                     const int b = u % kBufs;
+                    // the scale exponent of this chunk's key means (read before the wait)
+                    const float fk = pow2f(-(int)__ldg(a.kexp + (long long)(rq.kb_base + c * kChunk) * bd.h_kv + h));
                     const bool got = mbar_wait(bar(B_TF + kBufs * w + b), (u / kBufs) & 1, abort_flag, a.status,
                                                a.wait_ns);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
@@ -402,7 +454,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                     tc_fence_before();
                     mbar_arrive(bar(B_TE + kBufs * w + b));
                     if (pass == 0) {
-                        float m4[4] = {m, -INFINITY, -INFINITY, -INFINITY};
+                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                         for (int sl = 0; sl < kChunk / 32; ++sl) {
                             const int J0 = c * kChunk + sl * 32;
@@ -410,12 +462,16 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                             for (int e = 0; e < 32; ++e)
                                 if (J0 + e < ncol) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sv[sl][e]));
                         }
-                        m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                        // the chunk's largest scaled logit, unscaled exactly (powers of two)
+                        m = fmaxf(m, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * pow2f(-fq) * fk);
                     } else {
-                        // exponents as paired FMAs: (s0, s1) * c2 - mc2 (an invalid row
-                        // has mc2 = +inf, so its terms are exactly 0); columns past
-                        // the row are masked only in its last, partial chunk
-                        const uint64_t cc = f2_pack(c2, c2), nm = f2_pack(-mc2, -mc2);
+                        // exponents as paired FMAs: (s0, s1) * c2 * 2^-(f+e) - mc2, the
+                        // scaled logits times an exact power-of-two correction of the
+                        // constant (an invalid row has mc2 = +inf, so its terms are
+                        // exactly 0); columns past the row are masked only in its
+                        // last, partial chunk
+                        const float c2c = c2q * fk;
+                        const uint64_t cc = f2_pack(c2c, c2c), nm = f2_pack(-mc2, -mc2);
 #pragma unroll
                         for (int sl = 0; sl < kChunk / 32; ++sl) {
                             const int J0 = c * kChunk + sl * 32;
@@ -557,21 +613,70 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
     }
 }
 
-// fp32 block means -> three bf16 terms (hi, mid, lo) whose sum carries 24
-// significant bits; rows past the last block are zero.
-__global__ void split_means_kernel(const float *__restrict__ km, __nv_bfloat16 *__restrict__ terms, long long n,
-                                   long long n_pad) {
-    for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n_pad;
-         k += (long long)gridDim.x * blockDim.x) {
-        const float x = k < n ? km[k] : 0.f;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-        const float r1 = x - __bfloat162float(hi);
-        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-        const float r2 = r1 - __bfloat162float(mid);
-        terms[k] = hi;
-        terms[n_pad + k] = mid;
-        terms[2 * n_pad + k] = __float2bfloat16_rn(r2);
+// fp32 block means -> the score kernel's operands.  One CTA per chunk of 128
+// blocks of a request (from its first block) and kv head: the chunk's largest
+// magnitude sets the power of two 2^e (fp16_scale_exp), and
+//   kmean * 2^e = hi + lo,  hi = fp16(kmean * 2^e),  lo = fp16(kmean * 2^e - hi)
+// (the difference is exact in fp32; together 22 significant bits).  e goes to
+// kexp at [the chunk's first block][h].  Term t of block row k, head h, starts
+// at terms + t * n_pad + (k * h_kv + h) * d; rows past the last request's
+// blocks (up to rows_pad) are zero.
+constexpr int kSplitThreads = 256;
+__global__ void __launch_bounds__(kSplitThreads)
+split_means_kernel(const __grid_constant__ BatchDesc bd, const float *__restrict__ km, __half *__restrict__ terms,
+                   int8_t *__restrict__ kexp, long long n_pad, int rows_pad) {
+    int b = blockIdx.x, r = 0;
+    for (; r < bd.batch; ++r) {
+        const int nc = (bd.req[r].nkb + 127) / 128;
+        if (b < nc) break;
+        b -= nc;
     }
+    if (r == bd.batch) return;
+    const ReqDesc &rq = bd.req[r];
+    const int h = blockIdx.y;
+    const int row0 = rq.kb_base + b * 128;
+    const int nrow = min(128, rq.nkb - b * 128);
+    const int col = (threadIdx.x % 32) * 4;          // four dims
+    const int rw = threadIdx.x / 32;                 // rows rw, rw + 8, ...
+    float4 v[16];
+    float mx = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int rr = rw + 8 * k;
+        v[k] = rr < nrow ? __ldg(reinterpret_cast<const float4 *>(km + ((long long)(row0 + rr) * bd.h_kv + h) * kHeadDim + col))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
+    }
+    __shared__ float red[kSplitThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = mx;
+    __syncthreads();
+    mx = red[0];
+#pragma unroll
+    for (int k = 1; k < kSplitThreads / 32; ++k) mx = fmaxf(mx, red[k]);
+    const int e = fp16_scale_exp(__float_as_uint(mx));
+    const float sf = pow2f(e);
+    const bool last = r == bd.batch - 1;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int rr = rw + 8 * k;
+        if (rr >= nrow && !(last && row0 + rr < rows_pad)) continue;
+        const float x[4] = {v[k].x * sf, v[k].y * sf, v[k].z * sf, v[k].w * sf};
+        uint32_t hw[2], lw[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const __half2 hi = __floats2half2_rn(x[2 * q], x[2 * q + 1]);
+            const float2 hf = __half22float2(hi);
+            const __half2 lo = __floats2half2_rn(x[2 * q] - hf.x, x[2 * q + 1] - hf.y);
+            hw[q] = *reinterpret_cast<const uint32_t *>(&hi);
+            lw[q] = *reinterpret_cast<const uint32_t *>(&lo);
+        }
+        const long long o = ((long long)(row0 + rr) * bd.h_kv + h) * kHeadDim + col;
+        *reinterpret_cast<uint2 *>(terms + o) = make_uint2(hw[0], hw[1]);
+        *reinterpret_cast<uint2 *>(terms + n_pad + o) = make_uint2(lw[0], lw[1]);
+    }
+    if (threadIdx.x == 0) kexp[(long long)row0 * bd.h_kv + h] = (int8_t)e;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -598,7 +703,7 @@ bool map3(CUtensorMap *m, const void *base, long long n1, long long n2, long lon
     cuuint64_t strides[2] = {(cuuint64_t)(s1 * 2), (cuuint64_t)(s2 * 2)};
     cuuint32_t box[3] = {64, 1, (cuuint32_t)box2};
     cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -616,21 +721,26 @@ size_t score_tc_smem_bytes(int max_nkb) { return ScoreCfg<128>::smem_bytes(max_n
 
 cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
                             long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
-                            float *score, __nv_bfloat16 *terms, int *status, unsigned long long wait_ns,
+                            float *score, void *terms_ws, int *status, unsigned long long wait_ns,
                             cudaStream_t st, const ScoreSelect *sel, bool head_union) {
     const int rows_pad = score_tc_rows_pad(bd);
-    const long long n = (long long)bd.total_kb * bd.h_kv * kHeadDim;
     const long long n_pad = (long long)rows_pad * bd.h_kv * kHeadDim;
-    split_means_kernel<<<512, 256, 0, st>>>(k_mean, terms, n, n_pad);
+    __half *terms = static_cast<__half *>(terms_ws);
+    int8_t *kexp = static_cast<int8_t *>(terms_ws) + score_tc_kexp_offset(bd);
+    int chunks = 0;
+    for (int r = 0; r < bd.batch; ++r) chunks += (bd.req[r].nkb + 127) / 128;
+    if (chunks > 0) split_means_kernel<<<dim3(chunks, bd.h_kv), kSplitThreads, 0, st>>>(bd, k_mean, terms, kexp, n_pad, rows_pad);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap tmQ, tmM;
     (void)q_stride_head;
     const bool shared = score_tc_shared(bd.max_nkb);
-    if (!map3(&tmM, terms, bd.h_kv, 3LL * rows_pad, kHeadDim, (long long)bd.h_kv * kHeadDim, 128))
+    if (!map3(&tmM, terms, bd.h_kv, (long long)ScoreCfg<128>::kTerms * rows_pad, kHeadDim,
+              (long long)bd.h_kv * kHeadDim, 128))
         return cudaErrorInvalidValue;
     ScoreTcArgs a;
     a.score = score;
+    a.kexp = kexp;
     a.q8 = (const uint8_t *)q;
     a.q16 = (const __nv_bfloat16 *)q;
     a.q_stride_tok = q_stride_tok;

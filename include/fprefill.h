@@ -200,7 +200,7 @@ long long fp_score_offsets(const fp_problem *p, const fp_params *prm, long long 
  *     Score[I,J] = S'[J] / max_J' S'[J'] (so each row peaks at exactly 1).
  *     FP_SCORE_HEAD_UNION: the same per query head (its B queries alone),
  *     and Score[I,J] = max over the group's heads of those rows (still
- *     peaking at 1); rows over 4288 key blocks: FP_ERR_UNSUPPORTED.
+ *     peaking at 1); rows over 12480 key blocks: FP_ERR_UNSUPPORTED.
  *   ws: fp_discover_workspace_size() bytes (status header only).
  * ------------------------------------------------------------------------- */
 size_t fp_discover_workspace_size(const fp_problem *p, const fp_params *prm);

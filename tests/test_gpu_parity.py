@@ -442,18 +442,18 @@ def test_dim_major_value_cache(dtype, page):
 
 @pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
 def test_long_rows_on_the_tensor_cores_with_shared_column_sums(dtype):
-    """A 2700-block request (345,600 tokens): past 1024 blocks the tensor-core
+    """A 3300-block request (422,400 tokens): past 3120 blocks the tensor-core
     score kernel keeps one column-sum array per head slot, added to with
     shared-memory atomics.  Sampled score rows (within 2e-6) and their index
     rows (exact outside the flagged band) against the oracle."""
     import oracle
     import torch
     from block_sparse_long_fp_gb300 import fprefill
-    L = 2700 * 128
+    L = 3300 * 128
     spec = synth.Spec("long-rows-tc", [(L, 0)], 8, 1, page_size=128, layout="shuffled", dtype=dtype,
                       n_needles=2, logit_scale=4.0, config_id=78)
     case = synth.make_case(spec)
-    rows = np.array([0, 5, 1023, 1024, 2048, 2699])
+    rows = np.array([0, 5, 1023, 1024, 2048, 3120, 3299])
     ref = oracle.discover_and_select(case, row_subset=lambda r, nqb, hkv: rows)
     layer = fprefill.layer_from_case(case)
     k_mean, v_mean, score = layer.discover()
@@ -468,18 +468,18 @@ def test_long_rows_on_the_tensor_cores_with_shared_column_sums(dtype):
 
 @pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
 def test_rows_past_the_tensor_core_limit_use_the_fp32_score_kernel(dtype):
-    """A 563,200-token request (4400 key blocks) is past the tensor-core score
-    kernel's shared-memory limit (4288 blocks, with one column-sum array per
-    head slot past 1024): its scores come from the fp32 CUDA-core kernel.
+    """A 1,612,800-token request (12600 key blocks) is past the tensor-core
+    score kernel's shared-memory limit (12480 blocks, with one column-sum array
+    per head slot past 3120): its scores come from the fp32 CUDA-core kernel.
     Sampled score rows and their index rows against the oracle."""
     import oracle
     import torch
     from block_sparse_long_fp_gb300 import fprefill
-    L = 4400 * 128
+    L = 12600 * 128
     spec = synth.Spec("long-rows", [(L, 0)], 2, 1, page_size=128, layout="shuffled", dtype=dtype,
                       n_needles=2, logit_scale=4.0, config_id=77)
     case = synth.make_case(spec)
-    rows = np.array([0, 5, 700, 2048, 4399])
+    rows = np.array([0, 5, 700, 4096, 12599])
     ref = oracle.discover_and_select(case, row_subset=lambda r, nqb, hkv: rows)
     layer = fprefill.layer_from_case(case)
     k_mean, v_mean, score = layer.discover()
