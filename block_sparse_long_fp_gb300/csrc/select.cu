@@ -395,9 +395,15 @@ cudaError_t launch_select(const BatchDesc &bd, float alpha, int sink_blocks, int
         if (cudaMemsetAsync(row_ptr, 0, sizeof(int), st) != cudaSuccess) return cudaGetLastError();
         return cudaMemsetAsync(nnz, 0, sizeof(int), st);
     }
-    // a new epoch per call: look-back states of earlier calls read as empty
+    // a new epoch per call: look-back states of earlier calls read as empty.
+    // A graph replays the epoch it captured, so a call being captured clears
+    // the states instead (a memset node ahead of the kernel in the graph).
     static std::atomic<unsigned> calls{0};
     const unsigned epoch = (calls.fetch_add(1u) % 0x3ffffffeu) + 1u;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return cudaGetLastError();
+    if (cap != cudaStreamCaptureStatusNone && cudaMemsetAsync(lb_state, 0, select_state_bytes(bd), st) != cudaSuccess)
+        return cudaGetLastError();
     const int grid = (bd.total_rows + 7) / 8;
     select_kernel<<<grid, 256, 0, st>>>(bd, a, score, static_cast<unsigned long long *>(lb_state), epoch, row_ptr,
                                         col_idx, col_capacity, nnz, dense_mask, status, wait_ns);
