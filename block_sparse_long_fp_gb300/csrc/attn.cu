@@ -31,15 +31,14 @@
 //  * item list of a unit: the kept blocks (CSR row, ascending), then the
 //    tiles of block means that contain at least one skipped block; the dense
 //    path walks J = 0..I with no mean tiles;
-//  * a mean token's logit goes into the exponent, and one bf16 term of the key
-//    means moves it by up to 2^-9 * scale * sum_c |q_c kmean_c| (e4m3: 2^-4),
-//    so the key means enter S as two terms, hi + lo.  An e4m3 mean tile packs
-//    both 16 KB terms of 128 blocks into its K slot, and its S takes 4 more
-//    MMAs.  A bf16 mean tile covers 64 blocks: K slot rows 0..63 hold their hi
-//    terms and rows 64..127 their lo terms, the S MMAs are those of any tile,
-//    and the softmax adds column c + 64 to column c.  (Extra MMA code in the
-//    MMA thread, wherever placed, made that thread spill around every MMA and
-//    slowed every launch, dense ones included, by 10-25%.)
+//  * a mean token's logit goes into the exponent, where one bf16 term of the
+//    key means would move it by up to 2^-9 * scale * sum_c |q_c kmean_c| (e4m3:
+//    2^-4).  A mean tile covers 128 blocks.  e4m3 takes the key means as two
+//    terms, hi + lo, both 16 KB tiles in its K slot (4 more MMAs).  bf16 takes
+//    them as one fp16 term (2^-12) scaled by a power of two per tile and kv
+//    head, against queries converted in place to fp16 once the unit's kept
+//    blocks are done with them (exact, under a power-of-two scale per row);
+//    the exponent's constant undoes both scales.
 // Every mbarrier wait is bounded (status FP_ERR_TIMEOUT instead of a hang).
 #include <stdio.h>
 #include <stdlib.h>
@@ -68,11 +67,14 @@ constexpr int kSmemK = 2 * kTileBytes;
 constexpr int kSmemV = 4 * kTileBytes;
 constexpr int kSmemCtl = 6 * kTileBytes;                   // 192 KB
 constexpr int kBitmapWords = FP_MAX_KEY_BLOCKS / 32;
-constexpr int kMaxCorrTiles = FP_MAX_KEY_BLOCKS / (kBlock / 2);   // bf16 mean tiles span 64 blocks
+constexpr int kMaxCorrTiles = FP_MAX_KEY_BLOCKS / kBlock;   // mean tiles span 128 blocks
 
 // BAR_DR: the MMA thread's drain before the CTA leaves
+// A bf16 unit whose first term is a mean tile: its queries land on BAR_QL,
+// the softmax threads convert their rows to fp16 and arrive on BAR_QC, and one
+// of them then completes BAR_Q for the MMA thread
 enum { BAR_Q = 0, BAR_QE = 1, BAR_KF = 2, BAR_KE = 4, BAR_VF = 6, BAR_VE = 8, BAR_SF = 10, BAR_PF = 12,
-       BAR_OF = 14, BAR_MF = 16, BAR_ME = 18, BAR_DR = 20, NUM_BARS = 21 };
+       BAR_OF = 14, BAR_MF = 16, BAR_ME = 18, BAR_DR = 20, BAR_QL = 21, BAR_QC = 22, NUM_BARS = 23 };
 // arrivals on a metadata-empty barrier: the TMA thread, the MMA thread and
 // one lane of each of the eight softmax warps
 constexpr int kMetaConsumers = 10;
@@ -97,6 +99,41 @@ constexpr int kSmemAttn = kSmemMeta + 2 * (int)sizeof(UnitMeta) + 1024;
 static_assert(NUM_BARS * 8 + 8 <= 256, "control block");
 static_assert(sizeof(UnitMeta) % 16 == 0, "metadata buffers");
 
+// Row `row` of a 128 x 128 bf16 query tile in shared memory (two 64-column
+// halves, 128-byte rows, swizzled within each row) converted in place to fp16
+// under the row's own power-of-two scale 2^f: exact, since bf16 carries 8
+// significant bits and the scale puts the row's largest magnitude just under
+// fp16's largest value.  Returns 2^-f, which undoes the scale in the exponent.
+// The conversion is elementwise, so the swizzle does not matter; a lane starts
+// at the chunk its row number picks, so the 32 rows of a warp spread over the
+// banks.
+__device__ __noinline__ float q_to_f16(uint32_t tile, int row) {
+    // two passes over the row (the maximum, then the conversion), so that few
+    // registers are live: the control warps run it under a small budget
+    auto addr = [&](int c) { return tile + (c >> 3) * kHalfBytes + row * 128 + (((c & 7) + row) & 7) * 16; };
+    uint32_t mx2 = 0u;                             // bf16 bit patterns without the sign order like values
+#pragma unroll 4
+    for (int c = 0; c < 16; ++c) {
+        const uint4 w = ld_shared_v4(addr(c));
+        mx2 = __vmaxu2(__vmaxu2(mx2, w.x & 0x7fff7fffu),
+                       __vmaxu2(w.y & 0x7fff7fffu, __vmaxu2(w.z & 0x7fff7fffu, w.w & 0x7fff7fffu)));
+    }
+    const uint32_t mx16 = (mx2 >> 16) > (mx2 & 0xffffu) ? (mx2 >> 16) : (mx2 & 0xffffu);
+    const int f = fp16_scale_exp(mx16 << 16);
+    const float sf = pow2f(f);
+    auto cvt = [&](uint32_t x) {
+        const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x));
+        const __half2 h = __floats2half2_rn(v.x * sf, v.y * sf);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    };
+#pragma unroll 4
+    for (int c = 0; c < 16; ++c) {
+        const uint4 w = ld_shared_v4(addr(c));
+        st_shared_v4(addr(c), make_uint4(cvt(w.x), cvt(w.y), cvt(w.z), cvt(w.w)));
+    }
+    return pow2f(-f);
+}
+
 struct AttnArgs {
     const int *row_ptr;       // null in dense mode
     const int *col_idx;
@@ -112,7 +149,8 @@ struct AttnArgs {
     float *part_o;            // n_split > 1: fp32 partial outputs [n_split, total_q, h_q, d]
     float *part_lse;          // n_split > 1: partial LSEs [n_split, h_q, total_q]
     int mean_corr;
-    int mean_rows;            // row offset of the lo term of the key means
+    int mean_rows;            // row offset of the lo term of the key means (e4m3)
+    const int8_t *kexp;       // bf16: scale exponent of each mean tile's key means, at [tile's first block][h]
     float scale_log2;         // softmax scale * log2(e)
     const float *q_scale;     // e4m3 only: per query head / kv head scales
     const float *k_scale;
@@ -174,7 +212,9 @@ __device__ __forceinline__ Unit decode_unit(const BatchDesc &bd, const AttnArgs 
 // residual lo = e4m3(256 p - hi) in the next 32 TMEM columns, through a second
 // PV pass: e4m3's 1/16 relative rounding of the largest weights drops to
 // about 1/256
-template <bool kFp8, bool kLse, bool kVdm, bool kPlo = false>
+// kMean: the mean-tile code is compiled in (bf16 builds without it serve the
+// dense path and launches without the mean correction: less code in the loops).
+template <bool kFp8, bool kLse, bool kVdm, bool kPlo = false, bool kMean = true>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtensorMap tmQ,
             const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -201,7 +241,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
     // e4m3 in one 128-column box; smem slots are 32 KB either way
     constexpr int kT = kFp8 ? kTileBytes / 2 : kTileBytes;
     constexpr int kNH = kFp8 ? 1 : 2;
-    constexpr int kMeanSpan = kFp8 ? kBlock : kBlock / 2;   // blocks per mean tile
+    constexpr int kMeanSpan = kBlock;                        // blocks per mean tile
     const bool sparse = a.row_ptr != nullptr;
 
     // ---- set-up (once per CTA) ---------------------------------------------------
@@ -211,6 +251,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             if (k == BAR_PF || k == BAR_PF + 1) cnt = 128u;
             if (k == BAR_MF || k == BAR_MF + 1) cnt = 32u;
             if (k == BAR_ME || k == BAR_ME + 1) cnt = kMetaConsumers;
+            if (k == BAR_QC) cnt = 256u;
             mbar_init(bar(k), cnt);
         }
         st_shared_volatile(abort_flag, 0);
@@ -348,7 +389,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             int kq = 0;
             // for the drain after an abort (lane 0): the Q phase armed last (-1:
             // none), and the tile (0: K, 1: V) whose slot wait gave up, if one did
-            int q_ph = -1, fail_op = -1;
+            int q_ph = -1, fail_op = -1, q_bar = BAR_Q, nql = 0;
             for (int k = 0;; ++k) {
                 const int b = k & 1;
                 const UnitMeta &M = meta[b];
@@ -398,11 +439,15 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                         if (kq > 0 && !mbar_wait(bar(BAR_QE), (kq - 1) & 1, abort_flag, a.status, a.wait_ns)) good = false;
                         if (good) {
                             const int q_row0 = rq.q_off + U.il * kBlock;
-                            q_ph = kq & 1;
-                            mbar_expect_tx(bar(BAR_Q), 2 * kT);
+                            // a bf16 unit that starts with a mean tile: the converter
+                            // turns the queries to fp16 first, then completes BAR_Q
+                            const bool conv_first = !kFp8 && kMean && sparse && a.mean_corr && M.jb >= U.n_kept;
+                            q_bar = conv_first ? BAR_QL : BAR_Q;
+                            q_ph = conv_first ? (nql++ & 1) : (kq & 1);
+                            mbar_expect_tx(bar(q_bar), 2 * kT);
                             for (int t = 0; t < 2; ++t)
                                 for (int hf = 0; hf < kNH; ++hf)
-                                    tma_load_3d(sbase + kSmemQ + t * kTileBytes + hf * kHalfBytes, &tmQ, bar(BAR_Q),
+                                    tma_load_3d(sbase + kSmemQ + t * kTileBytes + hf * kHalfBytes, &tmQ, bar(q_bar),
                                                 hf * 64, U.hq0 + t, q_row0);
                         }
                     }
@@ -420,7 +465,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                             z_cur = row_of(pg_n, off_n);
                             look(j + per, pg_n, off_n);
                         }
-                        const bool kept = j < U.n_kept;
+                        const bool kept = !kMean || j < U.n_kept;
                         int zs[8];
 #pragma unroll
                         for (int sub = 0; sub < 8; ++sub)
@@ -473,19 +518,11 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                                         tma_load_3d(dst + kHalfBytes, tm, full, 0, U.h,
                                                     (op == 0 ? a.mean_rows : 0) + rq.kb_base + c * kBlock);
                                 } else {
-                                    // bf16 mean tile of 64 blocks: K slot rows 0..63 <- the hi terms
-                                    // of their key means, rows 64..127 <- the lo terms; V slot <- the
-                                    // value means (rows 64..127 get zero weight)
+                                    // bf16 mean tile: K slot <- the scaled fp16 key means of its 128
+                                    // blocks, V slot <- the bf16 value means
                                     const int row0 = rq.kb_base + c * kMeanSpan;
-                                    for (int hf = 0; hf < kNH; ++hf) {
-                                        if (op == 0) {
-                                            tma_load_3d(dst + hf * kHalfBytes, &tmKm, full, hf * 64, U.h, row0);
-                                            tma_load_3d(dst + hf * kHalfBytes + kMeanSpan * 128, &tmKm, full, hf * 64, U.h,
-                                                        a.mean_rows + row0);
-                                        } else {
-                                            tma_load_3d(dst + hf * kHalfBytes, &tmVm, full, hf * 64, U.h, row0);
-                                        }
-                                    }
+                                    for (int hf = 0; hf < kNH; ++hf)
+                                        tma_load_3d(dst + hf * kHalfBytes, op == 0 ? &tmKm : &tmVm, full, hf * 64, U.h, row0);
                                 }
                             }
                         }
@@ -500,7 +537,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             // after an abort, the copies armed last land before the CTA leaves
             // (otherwise every copy has been consumed already)
             if (lane == 0 && ld_shared_volatile(abort_flag)) {
-                if (q_ph >= 0) mbar_wait_drain(bar(BAR_Q), q_ph);
+                if (q_ph >= 0) mbar_wait_drain(bar(q_bar), q_ph);
                 // items before `it` were armed in full, except the one whose slot
                 // wait gave up: its K only when the V wait was the one that gave up
                 const int nk = fail_op == 0 ? (int)it - 1 : (int)it;
@@ -514,6 +551,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             // ================= MMA issuer =================
             constexpr uint32_t idS = kFp8 ? idesc_e4m3(128, 128, false) : idesc_bf16(128, 128, false);
             constexpr uint32_t idPV = kFp8 ? idesc_e4m3(128, 128, true) : idesc_bf16(128, 128, true);
+            constexpr uint32_t idS16 = idesc_f16(128, 128, false);   // bf16 mean tiles: fp16 queries and keys
             constexpr int kKSteps = kFp8 ? 4 : 8;                // K = 32 (e4m3) or 16 (bf16) per MMA
             constexpr int kKeysPerStep = kFp8 ? 32 : 16;
             // descriptors differ only in the start address: add offsets (in 16-byte units)
@@ -521,16 +559,17 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             const uint64_t kdesc = smem_desc_sw128(sbase + kSmemK, 16, 1024);
             const uint64_t vdesc = smem_desc_sw128(sbase + kSmemV, kFp8 ? 16 : kHalfBytes, 1024);
             const uint64_t kvdesc = smem_desc_sw128(sbase + kSmemV, 16, 1024);   // K-major V tiles (kVdm)
-            // two: an e4m3 mean tile, whose keys come as hi + lo terms (the lo
-            // tile sits in the upper half of the slot)
+            // two: a mean tile.  e4m3: its keys come as hi + lo terms (the lo tile
+            // sits in the upper half of the slot); bf16: queries and keys are fp16
             auto issue_S = [&](int t, int s, bool two) {
                 const uint64_t qd = qdesc + ((t * kTileBytes) >> 4);
                 const uint64_t kd = kdesc + ((s * kTileBytes) >> 4);
+                const uint32_t id = !kFp8 && two ? idS16 : idS;
 #pragma unroll
                 for (int kk = 0; kk < kKSteps; ++kk) {
                     const uint32_t off = (kFp8 ? kk * 32 : (kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
                     if constexpr (kFp8) mma_ss_f8(tmem + t * 256, qd + off, kd + off, idS, kk > 0);
-                    else mma_ss(tmem + t * 256, qd + off, kd + off, idS, kk > 0);
+                    else mma_ss(tmem + t * 256, qd + off, kd + off, id, kk > 0);
                 }
                 if constexpr (kFp8) {
                     if (two) {
@@ -559,11 +598,8 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     return;
                 }
                 const uint64_t vd = vdesc + ((s * kTileBytes) >> 4);
-                // a bf16 mean tile's P is zero past column 64: half the steps
-                const int nsteps = (!kFp8 && !kept) ? kPvSteps / 2 : kPvSteps;
 #pragma unroll
                 for (int kk = 0; kk < kPvSteps; ++kk) {
-                    if (kk >= nsteps) break;
                     const uint64_t b = vd + ((kk * kKeysPerStep * 128) >> 4);
                     if constexpr (kFp8) mma_ts_f8(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, b, idPV, (acc || kk > 0));
                     else mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, b, idPV, (acc || kk > 0));
@@ -645,7 +681,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
         const uint32_t tS = lane_base + t * 256;
         const uint32_t tO = tS + 128;
         uint32_t it = 0;
-        int kq = 0;
+        int kq = 0, nqc = 0;                          // nqc: units whose queries this role converted first
         for (int k = 0; !dead; ++k) {
             const int b = k & 1;
             const UnitMeta &M = meta[b];
@@ -693,8 +729,26 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             // the smaller weights carry e4m3 rounding.
             constexpr float kTau = kFp8 ? 0.f : 8.f;
             const int jb = M.jb;                          // this unit's part: terms jb ..
+            // bf16 mean tiles run on fp16 queries (2^f per row) and fp16 key means
+            // (2^e per tile); fqr = 2^-f undoes the row's scale.  A part that starts
+            // with a mean tile converts its queries here, once they land, and one
+            // thread then completes BAR_Q for the MMA thread
+            float fqr = 1.f;
+            if (!kFp8 && kMean && sparse && a.mean_corr && jb >= n_kept) {
+                const bool gq = mbar_wait(bar(BAR_QL), nqc & 1, abort_flag, a.status, a.wait_ns);
+                if (!__all_sync(0xffffffffu, gq)) break;
+                fqr = q_to_f16(sbase + kSmemQ + t * kTileBytes, rowt);
+                fence_proxy_async();                      // before the MMAs read the tile
+                mbar_arrive(bar(BAR_QC));
+                if (threadIdx.x == 128) {
+                    const bool gc = mbar_wait(bar(BAR_QC), nqc & 1, abort_flag, a.status, a.wait_ns);
+                    if (gc) mbar_arrive(bar(BAR_Q));
+                }
+                ++nqc;
+            }
             for (int jl = 0; jl < n_items; ++jl, ++it) {
                 const int j = jb + jl;
+                // a bf16 mean tile's key scale, loaded while the S MMA runs
                 const bool got = mbar_wait(bar(BAR_SF + t), it & 1, abort_flag, a.status, a.wait_ns);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }   // tcgen05.ld needs the whole warp
                 tc_fence_after();
@@ -712,39 +766,43 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
 #pragma unroll
                     for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]);
                 float bias = 0.f;
-                if (j < n_kept) {
+                float cs = csc;                           // logit scale of this term (log2 units)
+                // columns to keep, as four 32-bit words: the diagonal block keeps
+                // keys up to the query's position; a mean tile c (blocks kMeanSpan*c
+                // .. +kMeanSpan-1) keeps its skipped blocks J < I.  A skipped block
+                // J < I is full (only the request's last block can be short, and it
+                // is never before I), so its weight is n_J = 128: bias log2(128)
+                uint32_t w[4] = {~0u, ~0u, ~0u, ~0u};
+                bool masked = false;
+                if (!kMean || j < n_kept) {
                     // kept blocks ascend and J <= I: only the last one can be the
                     // diagonal block, the one that needs the causal mask
                     const int k0 = j == n_kept - 1 ? last_J * kBlock : 0;
-                    if (k0 + kBlock - 1 > pos) {          // the diagonal block: causal mask
+                    if (k0 + kBlock - 1 > pos) {
+                        masked = true;
 #pragma unroll
-                        for (int e = 0; e < 128; ++e)
-                            if (k0 + e > pos) x[e] = -INFINITY;
+                        for (int q = 0; q < 4; ++q) {
+                            const int n = pos - k0 - 32 * q + 1;          // keys of word q at or before pos
+                            w[q] = n <= 0 ? 0u : (n >= 32 ? ~0u : ((1u << n) - 1u));
+                        }
                     }
                 } else {
-                    // mean tile c covers blocks kMeanSpan*c .. +kMeanSpan-1; a skipped
-                    // block J < I is full (only the request's last block can be short,
-                    // and it is never before I), so its weight is n_J = 128: bias
-                    // log2(128).  bf16: column e < 64 holds q.hi of block 64c + e and
-                    // column e + 64 its q.lo
+                    masked = true;
                     const int c = M.corr[j - n_kept];
-                    uint32_t w[kMeanSpan / 32];
 #pragma unroll
-                    for (int q = 0; q < kMeanSpan / 32; ++q) {
+                    for (int q = 0; q < 4; ++q) {
                         const int J0 = c * kMeanSpan + 32 * q;
                         uint32_t valid = J0 >= I ? 0u : (I - J0 >= 32 ? 0xffffffffu : ((1u << (I - J0)) - 1u));
                         w[q] = valid ? (~M.bitmap[J0 >> 5] & valid) : 0u;   // 1 = skipped, before I
                     }
-                    if constexpr (!kFp8) {
-#pragma unroll
-                        for (int e = 0; e < 64; ++e) x[e] += x[e + 64];
-#pragma unroll
-                        for (int e = 64; e < 128; ++e) x[e] = -INFINITY;
-                    }
-#pragma unroll
-                    for (int e = 0; e < kMeanSpan; ++e)
-                        if (!((w[e >> 5] >> (e & 31)) & 1u)) x[e] = -INFINITY;
                     bias = 7.f;
+                    if constexpr (!kFp8)                      // both fp16 scales undone (powers of two)
+                        cs = csc * fqr * pow2f(-(int)__ldg(a.kexp + (long long)(rq.kb_base + c * kMeanSpan) * bd.h_kv + U.h));
+                }
+                if (masked) {
+#pragma unroll
+                    for (int e = 0; e < 128; ++e)
+                        if (!((w[e >> 5] >> (e & 31)) & 1u)) x[e] = -INFINITY;
                 }
                 // row max in independent chains of three-input max, then a tree:
                 // sixteen chains (at most four deep) for bf16; eight for e4m3,
@@ -769,7 +827,7 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     for (int e = 8; e < 128; e += 2) mx8[(e >> 1) & 7] = max3f(mx8[(e >> 1) & 7], x[e], x[e + 1]);
                     mxr = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
                 }
-                const float mx = mxr * csc + bias;                   // log2 units; -inf stays -inf
+                const float mx = mxr * cs + bias;                    // log2 units; -inf stays -inf
                 // grow the running max only when it rises by more than 2^8 (rarely);
                 // O is rescaled after P is written (x is dead by then), and the
                 // TMEM round trip runs warp-wide
@@ -785,27 +843,19 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 // exponents as paired FMAs: (s0, s1) * c + off.  P goes to TMEM
                 // first; the denominator is summed from the packed registers after
                 // the MMA has been told P is ready, off the critical path.
-                const uint64_t cc = f2_pack(csc, csc);
+                const uint64_t cc = f2_pack(cs, cs);
                 constexpr int kPk = kFp8 ? 32 : 64;   // packed words of P per row
                 uint32_t pk[kPk];
                 uint32_t pr[kPlo ? 32 : 1];           // kPlo: the residual term of P
                 if constexpr (!kFp8) {
                     const uint64_t oo = f2_pack(off, off);
-                    // a mean tile's columns 64..127 (its lo terms, folded into 0..63)
-                    // carry no weight
-                    const bool lo_half = j >= n_kept;
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
-                        if (half == 1 && lo_half) {
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) pk[32 + e] = 0u;
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) {
-                                float z0, z1;
-                                f2_unpack(f2_fma(f2_pack(x[64 * half + 2 * e], x[64 * half + 2 * e + 1]), cc, oo), z0, z1);
-                                pk[32 * half + e] = pack_bf16(fast_exp2(z0), fast_exp2(z1));
-                            }
+                        for (int e = 0; e < 32; ++e) {
+                            float z0, z1;
+                            f2_unpack(f2_fma(f2_pack(x[64 * half + 2 * e], x[64 * half + 2 * e + 1]), cc, oo), z0, z1);
+                            pk[32 * half + e] = pack_bf16(fast_exp2(z0), fast_exp2(z1));
                         }
                         tmem_st32(tS + 32 * half, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * half));
                     }
@@ -870,7 +920,11 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(bar(BAR_PF + t));
+                // bf16: after the last kept block of a part with mean tiles, this
+                // thread's query row goes to fp16 before P is handed over, so the
+                // tile's next S (a mean tile) reads fp16 queries
+                const bool conv = !kFp8 && kMean && sparse && a.mean_corr && j == n_kept - 1 && jl + 1 < n_items;
+                if (!conv) mbar_arrive(bar(BAR_PF + t));
                 // the denominator sums the same rounded weights the MMA multiplies,
                 // so the weights of a row sum to exactly one
                 float rs;
@@ -903,6 +957,11 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
                     rs = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
                 }
                 l += rs;
+                if (conv) {
+                    fqr = q_to_f16(sbase + kSmemQ + t * kTileBytes, rowt);
+                    fence_proxy_async();                  // before the MMAs read the tile
+                    mbar_arrive(bar(BAR_PF + t));
+                }
             }
             if (!ok) break;
             // epilogue: O / l -> bf16, LSE.  The unit's fields are decoded again
@@ -1097,22 +1156,70 @@ combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_
     if (lse && lane == 0) lse[(long long)head * total_q + tok] = den > 0.f ? mx + __logf(den) : -INFINITY;
 }
 
-// fp32 block means -> bf16 operands of the mean tiles; [n, n_pad) is zeroed.
-// The key means get two terms, hi at ao[k] and lo = bf16(x - hi) at
-// ao[n_pad + k] (16 significant bits together); the value means one.
-__global__ void to_bf16_kernel(const float *__restrict__ a, const float *__restrict__ b,
-                               __nv_bfloat16 *__restrict__ ao, __nv_bfloat16 *__restrict__ bo, long long n,
-                               long long n_pad) {
-    for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n_pad;
-         k += (long long)gridDim.x * blockDim.x) {
-        const float x = k < n ? a[k] : 0.f;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-        ao[k] = hi;
-        ao[n_pad + k] = __float2bfloat16_rn(x - __bfloat162float(hi));
-        bo[k] = __float2bfloat16_rn(k < n ? b[k] : 0.f);
-    }
+// fp32 block means -> the operands of the bf16 mean tiles.  One CTA per mean
+// tile (128 blocks of a request from its first block) and kv head: the key
+// means, scaled by the power of two 2^e that puts the tile's largest magnitude
+// in [2^14, 2^15), as fp16 (11 significant bits); e at kexp[tile's first
+// block][h]; the value means as bf16 (they enter O linearly).  Rows past the
+// last request's blocks (up to rows_pad) are zero, so the zero weights of
+// their columns meet finite values.
+// The scale exponents of the bf16 mean tiles sit in the workspace space of
+// the (e4m3-only) second key term: total_kb * h_kv bytes.
+static int8_t *mean_kexp(const AttnLaunch &L, const BatchDesc &bd) {
+    const size_t term = ((size_t)mean_rows(bd) * bd.h_kv * kHeadDim * 2 + 255) / 256 * 256;
+    return reinterpret_cast<int8_t *>(L.km16) + term;
 }
 
+constexpr int kMeanThreads = 256;
+__global__ void __launch_bounds__(kMeanThreads)
+mean_tiles_f16_kernel(const __grid_constant__ BatchDesc bd, const float *__restrict__ km, const float *__restrict__ vm,
+                      __half *__restrict__ ko, __nv_bfloat16 *__restrict__ vo, int8_t *__restrict__ kexp, int rows_pad) {
+    int b = blockIdx.x, r = 0;
+    for (; r < bd.batch; ++r) {
+        const int nc = (bd.req[r].nkb + kBlock - 1) / kBlock;
+        if (b < nc) break;
+        b -= nc;
+    }
+    if (r == bd.batch) return;
+    const ReqDesc &rq = bd.req[r];
+    const int h = blockIdx.y;
+    const int row0 = rq.kb_base + b * kBlock;
+    const int nrow = min(kBlock, rq.nkb - b * kBlock);
+    const bool last = r == bd.batch - 1;
+    const int col = (threadIdx.x % 32) * 4;          // four dims
+    const int rw = threadIdx.x / 32;                 // rows rw, rw + 8, ...
+    float4 v[16];
+    float mx = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int rr = rw + 8 * k;
+        v[k] = rr < nrow ? __ldg(reinterpret_cast<const float4 *>(km + ((long long)(row0 + rr) * bd.h_kv + h) * kHeadDim + col))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
+    }
+    __shared__ float red[kMeanThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = mx;
+    __syncthreads();
+    mx = red[0];
+#pragma unroll
+    for (int k = 1; k < kMeanThreads / 32; ++k) mx = fmaxf(mx, red[k]);
+    const int e = fp16_scale_exp(__float_as_uint(mx));
+    const float sf = pow2f(e);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int rr = rw + 8 * k;
+        if (rr >= nrow && !(last && row0 + rr < rows_pad)) continue;
+        const long long o = ((long long)(row0 + rr) * bd.h_kv + h) * kHeadDim + col;
+        const __half2 k01 = __floats2half2_rn(v[k].x * sf, v[k].y * sf), k23 = __floats2half2_rn(v[k].z * sf, v[k].w * sf);
+        *reinterpret_cast<uint2 *>(ko + o) =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&k01), *reinterpret_cast<const uint32_t *>(&k23));
+        const float4 w = rr < nrow ? __ldg(reinterpret_cast<const float4 *>(vm + o)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<uint2 *>(vo + o) = make_uint2(pack_bf16(w.x, w.y), pack_bf16(w.z, w.w));
+    }
+    if (threadIdx.x == 0) kexp[(long long)row0 * bd.h_kv + h] = (int8_t)e;
+}
 
 // fp32 block means -> e4m3 codes with the per-head K / V scales (block means
 // never exceed the largest |value| the scale maps to 448); [n, n_pad) is zeroed.
@@ -1174,7 +1281,7 @@ static int fail(const char *what, int code) {
 // (in elements) s1, s2; box (one 128-byte row of d, 1, box2), 128-byte
 // swizzle, zero fill out of bounds.
 static bool make_map(CUtensorMap *m, const void *base, long long n1, long long n2, long long s1, long long s2,
-                     int box2, bool fp8 = false) {
+                     int box2, bool fp8 = false, bool f16 = false) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) {
         fail("cuTensorMapEncodeTiled lookup", 0);
@@ -1185,7 +1292,7 @@ static bool make_map(CUtensorMap *m, const void *base, long long n1, long long n
     cuuint64_t strides[2] = {(cuuint64_t)(s1 * esz), (cuuint64_t)(s2 * esz)};
     cuuint32_t box[3] = {(cuuint32_t)(128 / esz), 1, (cuuint32_t)box2};
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+    CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : (f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16), 3,
                     const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS && debug_on())
@@ -1262,16 +1369,21 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
         // rows past the last block (padding up to one full 128-row box) are zero
         const long long n = (long long)bd.total_kb * bd.h_kv * kHeadDim;
         const long long n_pad = (long long)mean_rows(bd) * bd.h_kv * kHeadDim;
-        if (f8)
+        if (f8) {
             to_e4m3_kernel<<<1024, 256, 0, st>>>(L.k_mean, L.v_mean, L.k_scale, L.v_scale, (uint8_t *)L.km16,
                                                  (uint8_t *)L.vm16, n, n_pad, bd.h_kv);
-        else
-            to_bf16_kernel<<<1024, 256, 0, st>>>(L.k_mean, L.v_mean, L.km16, L.vm16, n, n_pad);
+        } else {
+            int tiles = 0;
+            for (int r = 0; r < bd.batch; ++r) tiles += (bd.req[r].nkb + kBlock - 1) / kBlock;
+            if (tiles > 0)
+                mean_tiles_f16_kernel<<<dim3(tiles, bd.h_kv), kMeanThreads, 0, st>>>(
+                    bd, L.k_mean, L.v_mean, reinterpret_cast<__half *>(L.km16), L.vm16, mean_kexp(L, bd), mean_rows(bd));
+        }
         if ((e = cudaGetLastError()) != cudaSuccess) return fail("mean conversion launch", (int)e);
-        // the key means' hi rows [0, mean_rows), lo rows [mean_rows, 2 mean_rows);
-        // bf16 mean tiles load each term as 64-row boxes
-        if (!make_map(&tmKm, L.km16, bd.h_kv, 2LL * mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim,
-                      f8 ? kBlock : kBlock / 2, f8))
+        // e4m3: the key means' hi rows [0, mean_rows), lo rows [mean_rows, 2 mean_rows);
+        // bf16: one fp16 term.  Both load 128-row boxes.
+        if (!make_map(&tmKm, L.km16, bd.h_kv, (f8 ? 2LL : 1LL) * mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim,
+                      kBlock, f8, !f8))
             return fail("mean K map", 0);
         if (!make_map(&tmVm, L.vm16, bd.h_kv, mean_rows(bd), kHeadDim, (long long)bd.h_kv * kHeadDim, kBlock, f8))
             return fail("mean V map", 0);
@@ -1280,7 +1392,7 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
         tmVm = tmV;
     }
     int *next_unit = L.work + units;
-    const int mean_span = use_means ? (f8 ? kBlock : kBlock / 2) : 0;
+    const int mean_span = use_means ? kBlock : 0;
     sched_kernel<<<bd.batch * bd.h_kv, kSchedThreads, 0, st>>>(bd, L.row_ptr, n_pairs, n_split, mean_span, L.work,
                                                               next_unit);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail("schedule launch", (int)e);
@@ -1300,6 +1412,7 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     a.part_lse = L.part_lse;
     a.mean_corr = use_means ? 1 : 0;
     a.mean_rows = mean_rows(bd);
+    a.kexp = use_means && !f8 ? mean_kexp(L, bd) : nullptr;
     a.scale_log2 = L.softmax_scale * 1.4426950408889634f;
     a.q_scale = L.q_scale;
     a.k_scale = L.k_scale;
@@ -1313,10 +1426,10 @@ int launch_attn(const AttnLaunch &L, cudaStream_t st) {
     auto kern = L.v_dim_major
                     ? (f8 ? (plo ? (want_lse ? attn_kernel<true, true, true, true> : attn_kernel<true, false, true, true>)
                                  : (want_lse ? attn_kernel<true, true, true> : attn_kernel<true, false, true>))
-                          : attn_kernel<false, false, true>)
+                          : (use_means ? attn_kernel<false, false, true> : attn_kernel<false, false, true, false, false>))
                     : (f8 ? (plo ? (want_lse ? attn_kernel<true, true, false, true> : attn_kernel<true, false, false, true>)
                                  : (want_lse ? attn_kernel<true, true, false> : attn_kernel<true, false, false>))
-                          : attn_kernel<false, false, false>);
+                          : (use_means ? attn_kernel<false, false, false> : attn_kernel<false, false, false, false, false>));
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttn)) != cudaSuccess)
         return fail("attention smem attribute", (int)e);
     // persistent: one CTA per SM (the shared memory admits one), never more than units

@@ -15,6 +15,21 @@ namespace fp {
 constexpr int kBlock = 128;     // tokens per query / key block
 constexpr int kHeadDim = 128;   // d
 
+// 2^e as a float, for |e| <= 126
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// The power-of-two exponent that brings a largest magnitude (its fp32 bit
+// pattern) into [2^14, 2^15): under fp16's largest finite value, with 2^29
+// of range below it, so that fp16 holds bf16 values and e4m3 codes exactly and
+// the two fp16 terms of an fp32 value carry 22 significant bits.  0 for a zero
+// (or subnormal) maximum; clamped so that 2^e and 2^-e stay normal floats.
+__host__ __device__ __forceinline__ int fp16_scale_exp(uint32_t max_bits) {
+    const int E = (int)((max_bits >> 23) & 0xffu);
+    if (E == 0) return 0;
+    const int e = 141 - E;
+    return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
+
 // One request of a varlen batch, as every kernel sees it (computed on the
 // host from the host descriptors).
 struct ReqDesc {

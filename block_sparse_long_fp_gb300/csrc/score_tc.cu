@@ -138,19 +138,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// 2^e as a float, for |e| <= 126
-__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
-
-// The power-of-two exponent that brings a largest magnitude (its fp32 bit
-// pattern) into [2^14, 2^15): under fp16's largest finite value, with 2^29
-// of range below it.  0 for a zero (or subnormal) maximum; clamped so that
-// 2^e and 2^-e stay normal floats.
-__host__ __device__ __forceinline__ int fp16_scale_exp(uint32_t max_bits) {
-    const int E = (int)((max_bits >> 23) & 0xffu);
-    if (E == 0) return 0;
-    const int e = 141 - E;
-    return e < -100 ? -100 : (e > 100 ? 100 : e);
-}
 
 // Column sums of a 32x32 block held one row per lane (v[c] = column c of
 // this lane's row): after the butterfly, lane L holds the sum of column L.
