@@ -22,12 +22,15 @@ def built():
 
 
 def full_parity(spec, alpha=0.1, mean_corr=True, rows_per_request=None, max_abs=None, mean_abs=None,
-                lse_abs=2e-2, select=None, v_layout=0):
+                lse_abs=2e-2, select=None, v_layout=0, case_fn=None):
     """select: {select_rule, top_k, top_p} for the top-k / top-p ablations;
-    v_layout: the value cache's layout on the GPU (the oracle reads the same values)."""
+    v_layout: the value cache's layout on the GPU (the oracle reads the same values);
+    case_fn: changes the generated case before both sides see it."""
     import oracle
     from parity_util import BF16_MAX_ABS, BF16_MEAN_ABS
     case = synth.make_case(spec)
+    if case_fn is not None:
+        case_fn(case)
     sel = select or {}
     ref = oracle.discover_and_select(case, alpha=alpha, rule=sel.get("select_rule", 0), top_k=sel.get("top_k", 0),
                                      top_p=sel.get("top_p", 0.0), head_union=sel.get("score_mode", 0) == 1)
@@ -206,8 +209,9 @@ def test_topk_topp_selection_ablations(select, mean_corr):
     """The top-k and top-p rules (ablations of the max threshold): the GPU's
     index equals the oracle's outside the flagged boundary band, and the
     attention on it matches.  With one kept block per row (k = 1) a row is
-    nearly all mean tokens: the mean tiles' keys enter the MMA as two bf16
-    terms, so their logits keep the accuracy of the kept blocks'."""
+    nearly all mean tokens: the mean tiles' keys enter the MMA in fp16 (11
+    significant bits, against fp16 queries), so their logits err by 2^-12
+    relative, not the 2^-9 of one bf16 term."""
     spec = synth.Spec("sharp-8k", [(8192, 0)], 4, 1, page_size=64, layout="shuffled", n_needles=2,
                       logit_scale=8.0, config_id=1)
     full_parity(spec, rows_per_request=1500, select=select, mean_corr=mean_corr)
@@ -490,3 +494,41 @@ def test_rows_past_the_tensor_core_limit_use_the_fp32_score_kernel(dtype):
              row_ptr=row_ptr.cpu().numpy(), col_idx=col_idx.cpu().numpy())
     check_pool(case, g, ref)
     check_scores_and_index(case, g, ref)
+
+
+def _bf16_times_pow2(bits, e):
+    """bf16 bit patterns times 2^e, exactly: the exponent field moves by e
+    (zeros stay zero; every normal value stays normal)."""
+    b = bits.astype(np.int32)
+    ex = (b >> 7) & 0xff
+    ok = (ex > 0) & (ex < 255)
+    ne = ex + e
+    assert np.all((ne[ok] > 0) & (ne[ok] < 255))
+    return np.where(ok, (b & ~(0xff << 7)) | (ne << 7), b).astype(np.uint16)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_queries_and_keys_far_from_unit_scale(dtype):
+    """Queries times 2^-13 and keys times 2^13 (bf16 values, or the e4m3
+    per-head scales): every logit equals the unscaled case's, but the key
+    means reach past fp16's largest value and most query entries fall below
+    its normal range.  The score MMAs and the bf16 mean tiles take fp16
+    operands scaled by powers of two (per 128-block tile of key means, per
+    query row), so scores, index and outputs meet the same bounds."""
+    from parity_util import FP8_LSE_ABS, FP8_MAX_ABS
+    spec = synth.Spec("scaled-8k", [(8192, 0)], 4, 1, page_size=64, layout="shuffled", dtype=dtype, n_needles=2,
+                      logit_scale=6.0, config_id=5)
+
+    def scale(case):
+        if dtype == "bf16":
+            case.q = _bf16_times_pow2(case.q, -13)
+            case.k_cache = _bf16_times_pow2(case.k_cache, 13)
+        else:
+            case.q_scale = (case.q_scale * 2.0 ** -13).astype(np.float32)
+            case.k_scale = (case.k_scale * 2.0 ** 13).astype(np.float32)
+
+    fp8 = dtype == "e4m3"
+    r = full_parity(spec, rows_per_request=3000, case_fn=scale, max_abs=FP8_MAX_ABS if fp8 else None,
+                    mean_abs=6e-3 if fp8 else None, lse_abs=FP8_LSE_ABS if fp8 else 2e-2,
+                    select=dict(p_terms=2) if fp8 else None)
+    assert r["density"] < 0.8
