@@ -1170,7 +1170,7 @@ static int8_t *mean_kexp(const AttnLaunch &L, const BatchDesc &bd) {
     return reinterpret_cast<int8_t *>(L.km16) + term;
 }
 
-constexpr int kMeanThreads = 256;
+constexpr int kMeanThreads = 1024;
 __global__ void __launch_bounds__(kMeanThreads)
 mean_tiles_f16_kernel(const __grid_constant__ BatchDesc bd, const float *__restrict__ km, const float *__restrict__ vm,
                       __half *__restrict__ ko, __nv_bfloat16 *__restrict__ vo, int8_t *__restrict__ kexp, int rows_pad) {
@@ -1187,14 +1187,15 @@ mean_tiles_f16_kernel(const __grid_constant__ BatchDesc bd, const float *__restr
     const int nrow = min(kBlock, rq.nkb - b * kBlock);
     const bool last = r == bd.batch - 1;
     const int col = (threadIdx.x % 32) * 4;          // four dims
-    const int rw = threadIdx.x / 32;                 // rows rw, rw + 8, ...
-    float4 v[16];
+    const int rw = threadIdx.x / 32;                 // rows rw, rw + 32, ...
+    float4 v[4], w[4];                               // key and value means of rows rw + 32 k
     float mx = 0.f;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const int rr = rw + 8 * k;
-        v[k] = rr < nrow ? __ldg(reinterpret_cast<const float4 *>(km + ((long long)(row0 + rr) * bd.h_kv + h) * kHeadDim + col))
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < 4; ++k) {
+        const int rr = rw + 32 * k;
+        const long long o = ((long long)(row0 + rr) * bd.h_kv + h) * kHeadDim + col;
+        v[k] = rr < nrow ? __ldg(reinterpret_cast<const float4 *>(km + o)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        w[k] = rr < nrow ? __ldg(reinterpret_cast<const float4 *>(vm + o)) : make_float4(0.f, 0.f, 0.f, 0.f);
         mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
     }
     __shared__ float red[kMeanThreads / 32];
@@ -1208,15 +1209,14 @@ mean_tiles_f16_kernel(const __grid_constant__ BatchDesc bd, const float *__restr
     const int e = fp16_scale_exp(__float_as_uint(mx));
     const float sf = pow2f(e);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const int rr = rw + 8 * k;
+    for (int k = 0; k < 4; ++k) {
+        const int rr = rw + 32 * k;
         if (rr >= nrow && !(last && row0 + rr < rows_pad)) continue;
         const long long o = ((long long)(row0 + rr) * bd.h_kv + h) * kHeadDim + col;
         const __half2 k01 = __floats2half2_rn(v[k].x * sf, v[k].y * sf), k23 = __floats2half2_rn(v[k].z * sf, v[k].w * sf);
         *reinterpret_cast<uint2 *>(ko + o) =
             make_uint2(*reinterpret_cast<const uint32_t *>(&k01), *reinterpret_cast<const uint32_t *>(&k23));
-        const float4 w = rr < nrow ? __ldg(reinterpret_cast<const float4 *>(vm + o)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<uint2 *>(vo + o) = make_uint2(pack_bf16(w.x, w.y), pack_bf16(w.z, w.w));
+        *reinterpret_cast<uint2 *>(vo + o) = make_uint2(pack_bf16(w[k].x, w[k].y), pack_bf16(w[k].z, w[k].w));
     }
     if (threadIdx.x == 0) kexp[(long long)row0 * bd.h_kv + h] = (int8_t)e;
 }

@@ -608,7 +608,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
 // kexp at [the chunk's first block][h].  Term t of block row k, head h, starts
 // at terms + t * n_pad + (k * h_kv + h) * d; rows past the last request's
 // blocks (up to rows_pad) are zero.
-constexpr int kSplitThreads = 256;
+constexpr int kSplitThreads = 1024;
 __global__ void __launch_bounds__(kSplitThreads)
 split_means_kernel(const __grid_constant__ BatchDesc bd, const float *__restrict__ km, __half *__restrict__ terms,
                    int8_t *__restrict__ kexp, long long n_pad, int rows_pad) {
@@ -624,12 +624,12 @@ split_means_kernel(const __grid_constant__ BatchDesc bd, const float *__restrict
     const int row0 = rq.kb_base + b * 128;
     const int nrow = min(128, rq.nkb - b * 128);
     const int col = (threadIdx.x % 32) * 4;          // four dims
-    const int rw = threadIdx.x / 32;                 // rows rw, rw + 8, ...
-    float4 v[16];
+    const int rw = threadIdx.x / 32;                 // rows rw, rw + 32, ...
+    float4 v[4];
     float mx = 0.f;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const int rr = rw + 8 * k;
+    for (int k = 0; k < 4; ++k) {
+        const int rr = rw + 32 * k;
         v[k] = rr < nrow ? __ldg(reinterpret_cast<const float4 *>(km + ((long long)(row0 + rr) * bd.h_kv + h) * kHeadDim + col))
                          : make_float4(0.f, 0.f, 0.f, 0.f);
         mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
@@ -646,8 +646,8 @@ split_means_kernel(const __grid_constant__ BatchDesc bd, const float *__restrict
     const float sf = pow2f(e);
     const bool last = r == bd.batch - 1;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const int rr = rw + 8 * k;
+    for (int k = 0; k < 4; ++k) {
+        const int rr = rw + 32 * k;
         if (rr >= nrow && !(last && row0 + rr < rows_pad)) continue;
         const float x[4] = {v[k].x * sf, v[k].y * sf, v[k].z * sf, v[k].w * sf};
         uint32_t hw[2], lw[2];
