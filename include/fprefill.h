@@ -261,9 +261,14 @@ fp_status fp_discover_select(const fp_problem *p, const fp_params *prm, float *k
  *   k_mean/v_mean: as produced by fp_discover (read only when mc = 1).
  *   out (device bf16 [total_q, h_q, d], contiguous).
  *   lse_opt (device fp32 [h_q, total_q], natural log; may be NULL).
- *   ws: fp_attn_workspace_size() bytes (work schedule, bf16 copies of the
- *   block means, and with split-KV the fp32 partial outputs and LSEs).
+ *   ws: fp_attn_workspace_size() bytes (work schedule, the tensor-core copies
+ *   of the block means, and with split-KV the fp32 partial outputs and LSEs).
  * A row with no term at all (an empty index row, no correction) yields O = 0.
+ * The mean tokens' logits run on the tensor cores: bf16 problems take the key
+ * means as fp16 (a power-of-two scale per 128-block tile and kv head) against
+ * the queries in fp16 (exact under a power-of-two scale per row), so a mean
+ * logit errs by about 2^-12 relative; e4m3 problems take them as two e4m3
+ * terms.
  *
  * Split-KV (the kept-count load balancing of the V2 popular article, "KV
  * split", for rows too long for the number of rows): with S = the split count
