@@ -18,23 +18,32 @@
 //    operands.
 //
 // One CTA per score row (request, query block I, kv head h).  The g query
-// heads of the group go in pairs (A, B), each head a 128-query tile (M = 128):
-//   pass 0: S = Q Kmean^T over the row's key blocks 0..I, 128 at a time -> row max
+// heads of the group go in pairs (A, B), each head a 128-query tile (M = 128),
+// and each pair takes two passes over the row's key blocks 0..I, 128 at a time:
+//   pass 0: S = Q Kmean^T -> row max
 //   pass 1: the same S again -> exp2((s - max) * scale * log2 e), summed down
 //           the 128 queries (a transpose-reduce across each warp's 32 rows)
 //           into per-warp column sums in shared memory;
 // then S' = the sum of all warps' column sums (fixed order) and the row is
-// divided by its maximum.  Warp 0 issues TMA loads (the two mean terms of a
-// chunk of key blocks, shared by both heads, in a ring of stages), warp 1
-// issues the MMAs, warpgroup A (warps 4-7) and warpgroup B (warps 8-11) each
-// own one head of the pair and its TMEM S buffers, one query row per thread,
-// so the two heads' row work overlaps.  A row warp pulls a whole chunk of S
-// into registers before it works on it, so the buffer is free for the next
-// MMA at once.  Each warpgroup also writes its head's query tile into TMEM,
-// where the MMA takes it as the A operand (the MMAs read only the mean terms
-// from shared memory); there are two query buffers, and the next pair's
-// queries (prefetched into L2 when the pair starts) go in at the start of
-// this pair's second pass, so the tensor cores never wait for them.
+// divided by its maximum.  The passes of consecutive pairs overlap: phase k
+// (k = 0 .. pairs) runs pass 0 of pair k and pass 1 of pair k - 1 chunk by
+// chunk, so the row warps' exponentials of one pair run while the tensor
+// cores compute the next pair's maxima, and each chunk of key means is loaded
+// once per phase.  Warp 0 issues TMA loads (the two mean terms of a chunk,
+// shared by both heads and both passes, in a ring of stages), warp 1 issues
+// the MMAs, warpgroup A (warps 4-7) and warpgroup B (warps 8-11) each own one
+// head slot of the pairs and its TMEM S buffer, one query row per thread.  A
+// row warp pulls a whole chunk of S into registers before it works on it, so
+// the buffer is free for the next MMA at once.  Each warpgroup also writes its
+// head's query tile into TMEM, where the MMA takes it as the A operand (the
+// MMAs read only the mean terms from shared memory); there are two query
+// buffers, one per pair in flight, and pair k's queries go in at the start of
+// phase k, once pair k - 2 is done.  While shared memory has room (rows of up
+// to 1072 blocks), warp 0 also stages each head slot's next query tile there
+// by TMA during the phase before, so a row thread reads its row from shared
+// memory (one row per thread straight from global memory touches 32 lines per
+// load instruction); longer rows read their queries from global memory,
+// prefetched into L2 one phase ahead.
 #include <type_traits>
 
 #include "common.cuh"
@@ -51,7 +60,7 @@ constexpr int kScThreads = 384;
 
 // Layout of one build of the kernel for a chunk of kChunk key blocks (MMA N;
 // also the span of one scale of the key means).
-template <int C>
+template <int C, bool kQs = false>
 struct ScoreCfg {
     static constexpr int kChunk = C;
     static constexpr int kTerms = 2;                           // fp16 terms of the key means
@@ -61,7 +70,11 @@ struct ScoreCfg {
     static constexpr int kStages = C == 64 ? 3 : 2;
     static constexpr int kTmemBufs = 2 * kBufs;
     static constexpr int kSmStage = 0;
-    static constexpr int kSmCtl = kSmStage + kStages * kStageBytes;
+    // kQs: the query tiles of the two head slots staged in shared memory by
+    // TMA (128 rows x 128 B per box, 128-byte swizzle; bf16 two boxes per tile)
+    static constexpr int kQTileBytes = 128 * kHeadDim * 2;
+    static constexpr int kSmQs = kSmStage + kStages * kStageBytes;
+    static constexpr int kSmCtl = kSmQs + (kQs ? 2 * kQTileBytes : 0);
     static constexpr int kSmAcc = kSmCtl + 512;                // column sums [8 or 2][max_nkb]
     // TMEM: the S buffers (kBufs per head slot), then the query tiles as MMA
     // A operands (128 rows x 128 fp16 = 64 columns each), two buffers of two
@@ -70,7 +83,9 @@ struct ScoreCfg {
     // barriers: Q full/empty per (buffer, head slot), stage full/empty, TMEM
     // full/empty per (head slot, S buffer)
     static constexpr int B_QF = 0, B_QE = 4, B_SF = 8, B_SE = 8 + kStages, B_TF = 8 + 2 * kStages;
-    static constexpr int B_TE = B_TF + 4, B_DR = B_TE + 4, B_N = B_DR + 1;   // B_DR: the MMAs' drain
+    static constexpr int B_TE = B_TF + 4, B_DR = B_TE + 4;                  // B_DR: the MMAs' drain
+    // kQs: query tile landed / read, per head slot
+    static constexpr int B_QL = B_DR + 1, B_QR = B_QL + 2, B_N = B_QR + 2;
     static_assert(kTmemQ + 256 <= 512, "TMEM budget");
     static_assert(B_N * 8 + 128 <= 512, "control block");
     // shared: one column-sum array per head slot instead of one per row warp
@@ -175,17 +190,20 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
 // (shared-memory atomics, so the order of the additions varies from run to
 // run) instead of one array each: rows past 3120 blocks (up to 12480) then
 // still fit.  Without it every sum is added in a fixed order.
-template <bool kFp8, int kCh, bool kShared>
+template <bool kFp8, int kCh, bool kShared, bool kQs>
 __global__ void __launch_bounds__(kScThreads, 1)
 score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmM, const ScoreTcArgs a) {
-    using Cfg = ScoreCfg<kCh>;
+    using Cfg = ScoreCfg<kCh, kQs>;
+    static_assert(!(kQs && kShared), "staged queries only with per-warp column sums");
     static_assert(kCh == 128, "the key means' scales span 128-block chunks");
-    constexpr int kChunk = Cfg::kChunk, kBufs = Cfg::kBufs, kTermBytes = Cfg::kTermBytes;
+    constexpr int kChunk = Cfg::kChunk, kTermBytes = Cfg::kTermBytes;
+    static_assert(Cfg::kBufs == 1, "one TMEM S buffer per head slot");
     constexpr int kStageBytes = Cfg::kStageBytes, kStages = Cfg::kStages, kSmStage = Cfg::kSmStage;
     constexpr int kSmCtl = Cfg::kSmCtl, kSmAcc = Cfg::kSmAcc, kTmemQ = Cfg::kTmemQ;
     constexpr int B_QF = Cfg::B_QF, B_QE = Cfg::B_QE, B_SF = Cfg::B_SF, B_SE = Cfg::B_SE;
     constexpr int B_TF = Cfg::B_TF, B_TE = Cfg::B_TE, B_DR = Cfg::B_DR, B_N = Cfg::B_N;
+    constexpr int B_QL = Cfg::B_QL, B_QR = Cfg::B_QR, kSmQs = Cfg::kSmQs;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned; derived from smem_raw by an offset, and the barriers
     // and the abort flag addressed in the shared window (no generic pointer
@@ -218,11 +236,11 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
     float *out = a.score ? a.score + row_off : nullptr;
 
     const int npairs = (g + 1) / 2;
-    const int steps_per_pair = 2 * nch;
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < B_N; ++k)
-            mbar_init(bar(k), ((k >= B_TE && k < B_TE + 4) || (k >= B_QF && k < B_QF + 4)) ? 128u : 1u);
+            mbar_init(bar(k), ((k >= B_TE && k < B_TE + 4) || (k >= B_QF && k < B_QF + 4) || (k >= B_QR && k < B_QR + 2))
+                                  ? 128u : 1u);
         st_shared_volatile(abort_flag, 0);
         *sync_ctr = 0u;
         fence_barrier_init();
@@ -240,11 +258,26 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
     if (warp < 4) {
         if (warp == 0 && lane == 0) {
             // ================= TMA producer =================
+            // phase k runs pass 0 of pair k and pass 1 of pair k - 1 (k = 0 .. npairs):
+            // each chunk of key means is loaded once per phase for both
             tma_prefetch_desc(&tmM);
+            // kQs: head slot w's query tile of pair p (128 query rows of head hq)
+            int nq[2] = {0, 0};                    // query tiles issued per head slot
+            auto load_q = [&](int p, int w) {
+                constexpr int kBoxes = kFp8 ? 1 : 2;
+                mbar_expect_tx(bar(B_QL + w), kBoxes * 128 * 128);
+                for (int hf = 0; hf < kBoxes; ++hf)
+                    tma_load_3d(sbase + kSmQs + w * Cfg::kQTileBytes + hf * 128 * 128, &tmQ, bar(B_QL + w), hf * 64,
+                                h * g + 2 * p + w, rq.q_off + il * kBlock);
+                ++nq[w];
+            };
+            if constexpr (kQs) {
+                tma_prefetch_desc(&tmQ);
+                for (int w = 0; w < (g > 1 ? 2 : 1); ++w) load_q(0, w);
+            }
             int step = 0;
-            for (int pr = 0; pr < npairs && !ld_shared_volatile(abort_flag); ++pr) {
-                for (int k = 0; k < steps_per_pair; ++k, ++step) {
-                    const int c = k % nch;
+            for (int k = 0; k <= npairs && !ld_shared_volatile(abort_flag); ++k) {
+                for (int c = 0; c < nch; ++c, ++step) {
                     const int s = step % kStages, use = step / kStages;
                     if (step >= kStages && !mbar_wait(bar(B_SE + s), (use - 1) & 1, abort_flag, a.status, a.wait_ns))
                         goto producer_done;
@@ -254,52 +287,67 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                         for (int hf = 0; hf < 2; ++hf)
                             tma_load_3d(dst + t * kTermBytes + hf * (kTermBytes / 2), &tmM, bar(B_SF + s), hf * 64, h,
                                         t * a.rows_pad + rq.kb_base + c * kChunk);
+                    // kQs: pair k + 1's queries, once the row warps have read pair k's
+                    // (early in phase k; the chunks armed so far keep the MMAs busy)
+                    if (kQs && c == (nch > 1 ? 1 : 0) && k + 1 < npairs)
+                        for (int w = 0; w < ((2 * k + 3 < g) ? 2 : 1); ++w) {
+                            if (!mbar_wait(bar(B_QR + w), k & 1, abort_flag, a.status, a.wait_ns)) goto producer_done;
+                            load_q(k + 1, w);
+                        }
                 }
             }
         producer_done:
             // after an abort, the copies of the last stages armed land before the
             // CTA leaves (otherwise the MMAs have consumed every stage already)
-            if (ld_shared_volatile(abort_flag))
+            if (ld_shared_volatile(abort_flag)) {
                 for (int j = step > kStages ? step - kStages : 0; j < step; ++j)
                     mbar_wait_drain(bar(B_SF + j % kStages), (j / kStages) & 1);
+                // each slot's last query tile (every earlier one was read)
+                for (int w = 0; w < 2; ++w)
+                    if (nq[w] > 0) mbar_wait_drain(bar(B_QL + w), (nq[w] - 1) & 1);
+            }
         } else if (warp == 1 && lane == 0) {
             // ================= MMA issuer =================
+            // per chunk of phase k: S of pass 1 of pair k - 1 for each head slot,
+            // then S of pass 0 of pair k, each slot's S into its own TMEM buffer
             constexpr uint32_t idS = idesc_f16(128, kChunk, false);
             int step = 0;
-            int uses[2] = {0, 0};                  // TMEM-buffer uses per head slot
-            for (int pr = 0; pr < npairs; ++pr) {
-                const int nw = (2 * pr + 1 < g) ? 2 : 1;
-                const int qb = pr & 1;             // query buffer of this pair
-                for (int w = 0; w < nw; ++w)
-                    if (!mbar_wait(bar(B_QF + 2 * qb + w), (pr >> 1) & 1, abort_flag, a.status, a.wait_ns))
-                        goto mma_done;
-                for (int k = 0; k < steps_per_pair; ++k, ++step) {
+            int uses[2] = {0, 0};                  // S productions per head slot
+            auto issue = [&](int w, int qb, uint64_t kd) -> bool {
+                const int u = uses[w]++;
+                if (u >= 1 && !mbar_wait(bar(B_TE + w), (u - 1) & 1, abort_flag, a.status, a.wait_ns)) return false;
+                tc_fence_after();
+                // descriptors differ only in the start address: add offsets (in 16-byte units)
+                const uint32_t dt = tmem + w * kChunk;
+                const uint32_t qt = tmem + kTmemQ + (2 * qb + w) * 64;   // A: 16 d-values per 8 columns
+#pragma unroll
+                for (int t = 0; t < Cfg::kTerms; ++t)
+#pragma unroll
+                    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                        const uint32_t boff = t * kTermBytes + (kk >> 2) * (kTermBytes / 2) + (kk & 3) * 32;
+                        mma_ts(dt, qt + kk * 8, kd + (boff >> 4), idS, (t | kk) != 0);
+                    }
+                tc_commit(bar(B_TF + w));
+                return true;
+            };
+            for (int k = 0; k <= npairs; ++k) {
+                const int n1 = k >= 1 ? ((2 * k - 1 < g) ? 2 : 1) : 0;     // head slots of pair k - 1
+                const int n0 = k < npairs ? ((2 * k + 1 < g) ? 2 : 1) : 0;  // head slots of pair k
+                for (int c = 0; c < nch; ++c, ++step) {
                     const int s = step % kStages;
                     if (!mbar_wait(bar(B_SF + s), (step / kStages) & 1, abort_flag, a.status, a.wait_ns)) goto mma_done;
-                    const uint32_t kb = sbase + kSmStage + s * kStageBytes;
-                    for (int w = 0; w < nw; ++w) {
-                        const int u = uses[w]++;
-                        const int b = u % kBufs;
-                        if (u >= kBufs && !mbar_wait(bar(B_TE + kBufs * w + b), ((u / kBufs) - 1) & 1, abort_flag, a.status,
-                                                 a.wait_ns))
+                    const uint64_t kd = smem_desc_sw128(sbase + kSmStage + s * kStageBytes, 16, 1024);
+                    for (int w = 0; w < n1; ++w)
+                        if (!issue(w, (k - 1) & 1, kd)) goto mma_done;
+                    if (c == nch - 1)                  // pair k - 1 is done with its query buffer
+                        for (int w = 0; w < n1; ++w) tc_commit(bar(B_QE + 2 * ((k - 1) & 1) + w));
+                    for (int w = 0; w < n0; ++w) {
+                        if (c == 0 && !mbar_wait(bar(B_QF + 2 * (k & 1) + w), (k >> 1) & 1, abort_flag, a.status, a.wait_ns))
                             goto mma_done;
-                        tc_fence_after();
-                        // descriptors differ only in the start address: add offsets (in 16-byte units)
-                        const uint64_t kd = smem_desc_sw128(kb, 16, 1024);
-                        const uint32_t dt = tmem + (kBufs * w + b) * kChunk;
-                        const uint32_t qt = tmem + kTmemQ + (2 * qb + w) * 64;   // A: 16 d-values per 8 columns
-#pragma unroll
-                        for (int t = 0; t < Cfg::kTerms; ++t)
-#pragma unroll
-                            for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                                const uint32_t boff = t * kTermBytes + (kk >> 2) * (kTermBytes / 2) + (kk & 3) * 32;
-                                mma_ts(dt, qt + kk * 8, kd + (boff >> 4), idS, (t | kk) != 0);
-                            }
-                        tc_commit(bar(B_TF + kBufs * w + b));
+                        if (!issue(w, k & 1, kd)) goto mma_done;
                     }
                     tc_commit(bar(B_SE + s));
                 }
-                for (int w = 0; w < nw; ++w) tc_commit(bar(B_QE + 2 * qb + w));
             }
         mma_done:
             if (ld_shared_volatile(abort_flag)) {   // after an abort, every MMA issued is done
@@ -340,12 +388,22 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
             const int hq = h * g + 2 * pr_q + w;
             const long long el = (long long)(rq.q_off + il * kBlock + rowt) * a.q_stride_tok + (long long)hq * a.q_stride_head;
             const uint32_t qdst = lane_base + kTmemQ + (2 * qb + w) * 64;
+            // kQs: this row of the staged tile, 16-byte piece j of each 128-byte
+            // box row at j ^ (row & 7) (128-byte swizzle)
+            const uint32_t qrow = sbase + kSmQs + w * Cfg::kQTileBytes + rowt * 128;
+            if constexpr (kQs) {
+                const bool got = mbar_wait(bar(B_QL + w), pr_q & 1, abort_flag, a.status, a.wait_ns);
+                if (!__all_sync(0xffffffffu, got)) return false;
+            }
             if constexpr (!kFp8) {
                 uint32_t qw[64];
                 const uint4 *src = reinterpret_cast<const uint4 *>(a.q16 + el);
 #pragma unroll
                 for (int v = 0; v < 16; ++v) {
-                    const uint4 c = row_valid ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                    uint4 c;
+                    if constexpr (kQs) c = ld_shared_v4(qrow + (v >> 3) * 128 * 128 + (((v & 7) ^ (rowt & 7)) << 4));
+                    else c = row_valid ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                    if (kQs && !row_valid) c = make_uint4(0, 0, 0, 0);
                     qw[4 * v] = c.x; qw[4 * v + 1] = c.y; qw[4 * v + 2] = c.z; qw[4 * v + 3] = c.w;
                 }
                 // the row's largest magnitude: bf16 bit patterns without the sign
@@ -353,6 +411,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                 uint32_t mx2 = 0u;
 #pragma unroll
                 for (int k = 0; k < 64; ++k) mx2 = __vmaxu2(mx2, qw[k] & 0x7fff7fffu);
+                if constexpr (kQs) mbar_arrive(bar(B_QR + w));   // read: the tile may be reloaded
                 const uint32_t mx16 = (mx2 >> 16) > (mx2 & 0xffffu) ? (mx2 >> 16) : (mx2 & 0xffffu);
                 const int f = fp16_scale_exp(mx16 << 16);
                 const float sf = pow2f(f);
@@ -365,13 +424,18 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                 tmem_st32(qdst + 32, *reinterpret_cast<const uint32_t(*)[32]>(qw + 32));
                 f_out = f;
             } else {
+                uint4 cq[8];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    if constexpr (kQs) cq[v] = row_valid ? ld_shared_v4(qrow + ((v ^ (rowt & 7)) << 4)) : make_uint4(0, 0, 0, 0);
+                    else cq[v] = row_valid ? __ldg(reinterpret_cast<const uint4 *>(a.q8 + el) + v) : make_uint4(0, 0, 0, 0);
+                }
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t qw[32];
-                    const uint4 *src = reinterpret_cast<const uint4 *>(a.q8 + el) + half * 4;
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
-                        const uint4 c = row_valid ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                        const uint4 c = cq[half * 4 + v];
                         const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
@@ -382,6 +446,7 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                     }
                     tmem_st32(qdst + half * 32, qw);
                 }
+                if constexpr (kQs) mbar_arrive(bar(B_QR + w));   // read: the tile may be reloaded
                 f_out = 0;
             }
             tmem_st_wait();
@@ -399,98 +464,106 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
             asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
             if constexpr (!kFp8) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + 128));
         };
-        int fq = 0, fq_next = 0;                          // row scale exponents (this pair, the next)
-        if (w < g) ok = put_queries(0, fq);
-        for (int pr = 0; pr < npairs && ok; ++pr) {
-            if (pr > 0) fq = fq_next;
-            // a slot without a head in this pair (odd g, last pair) has no passes;
-            // under the union of heads it still takes part in the pair's syncs
-            const bool has_head = 2 * pr + w < g;
-            if (!has_head && !a.head_union) break;
-            const int hq = h * g + 2 * pr + (has_head ? w : 0);
-            const bool next = 2 * (pr + 1) + w < g;       // this slot has a head in the next pair
-            if (next) prefetch_queries(pr + 1);
-            const float c2 = kFp8 ? a.scale_log2 * __ldg(a.q_scale + hq) : a.scale_log2;
-            const float c2q = c2 * pow2f(-fq);          // undoes the row's query scale
-            float m = -INFINITY;                        // the row's largest logit (unscaled)
-            float mc2 = 0.f;
-            for (int pass = 0; pass < 2 && ok && has_head; ++pass) {
-                if (pass == 1) {
-                    mc2 = !row_valid ? INFINITY : (m == -INFINITY ? 0.f : m * c2);
-                    // the next pair's queries go into the other buffer while this
-                    // pair's second pass keeps the tensor cores busy
-                    if (next && !put_queries(pr + 1, fq_next)) { ok = false; break; }
-                }
-                for (int c = 0; c < nch; ++c, ++u) {
-                    const int b = u % kBufs;
-                    // the scale exponent of this chunk's key means (read before the wait)
-                    const float fk = pow2f(-(int)__ldg(a.kexp + (long long)(rq.kb_base + c * kChunk) * bd.h_kv + h));
-                    const bool got = mbar_wait(bar(B_TF + kBufs * w + b), (u / kBufs) & 1, abort_flag, a.status,
-                                               a.wait_ns);
-                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        // phase k: this slot's head of pair k (pass 0: the row max) and of pair
+        // k - 1 (pass 1: the exponentials), chunk by chunk in the MMA's order
+        int fq = 0, fq_prev = 0;                          // row scale exponents (pair k, pair k - 1)
+        float m_prev = -INFINITY;                         // pair k - 1's row max (unscaled logits)
+        for (int k = 0; k <= npairs && ok; ++k) {
+            const bool has0 = k < npairs && 2 * k + w < g;
+            const bool has1 = k >= 1 && 2 * (k - 1) + w < g;
+            // a slot with no head left (odd g) stops; under the union of heads it
+            // still takes part in the pairs' syncs
+            if (!has0 && !has1 && !a.head_union) break;
+            if (has0) {
+                if (!kQs && 2 * (k + 1) + w < g) prefetch_queries(k + 1);
+                if (!put_queries(k, fq)) { ok = false; break; }
+            }
+            float c2q1 = 0.f, mc2 = 0.f;                // pass 1 of pair k - 1
+            if (has1) {
+                const float c2 = kFp8 ? a.scale_log2 * __ldg(a.q_scale + h * g + 2 * (k - 1) + w) : a.scale_log2;
+                c2q1 = c2 * pow2f(-fq_prev);            // undoes the row's query scale
+                mc2 = !row_valid ? INFINITY : (m_prev == -INFINITY ? 0.f : m_prev * c2);
+            }
+            const float fq0 = pow2f(-fq);
+            float m = -INFINITY;                        // pair k's row max
+            for (int c = 0; c < nch && (has0 || has1); ++c) {
+                // the scale exponent of this chunk's key means (read before the wait)
+                const float fk = pow2f(-(int)__ldg(a.kexp + (long long)(rq.kb_base + c * kChunk) * bd.h_kv + h));
+                // the next S of this slot, whole into registers; the buffer is then
+                // free for the next MMA while this warp works on the values
+                uint32_t sv[kChunk / 32][32];
+                auto pull = [&]() -> bool {
+                    const bool got = mbar_wait(bar(B_TF + w), u & 1, abort_flag, a.status, a.wait_ns);
+                    if (!__all_sync(0xffffffffu, got)) return false;
+                    ++u;
                     tc_fence_after();
-                    // the whole chunk into registers, then the buffer is free for
-                    // the next MMA while this warp works on the values
-                    const uint32_t colb = lane_base + (kBufs * w + b) * kChunk;
-                    uint32_t sv[kChunk / 32][32];
+                    const uint32_t colb = lane_base + w * kChunk;
 #pragma unroll
                     for (int sl = 0; sl < kChunk / 32; ++sl) tmem_ld32(colb + sl * 32, sv[sl]);
                     tmem_ld_wait();
 #pragma unroll
                     for (int sl = 0; sl < kChunk / 32; ++sl) reg_fence(sv[sl]);
                     tc_fence_before();
-                    mbar_arrive(bar(B_TE + kBufs * w + b));
-                    if (pass == 0) {
-                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    mbar_arrive(bar(B_TE + w));
+                    return true;
+                };
+                if (has1) {
+                    if (!pull()) { ok = false; break; }
+                    // exponents as paired FMAs: (s0, s1) * c2 * 2^-(f+e) - mc2, the
+                    // scaled logits times an exact power-of-two correction of the
+                    // constant (an invalid row has mc2 = +inf, so its terms are
+                    // exactly 0); columns past the row are masked only in its
+                    // last, partial chunk
+                    const float c2c = c2q1 * fk;
+                    const uint64_t cc = f2_pack(c2c, c2c), nm = f2_pack(-mc2, -mc2);
 #pragma unroll
-                        for (int sl = 0; sl < kChunk / 32; ++sl) {
-                            const int J0 = c * kChunk + sl * 32;
+                    for (int sl = 0; sl < kChunk / 32; ++sl) {
+                        const int J0 = c * kChunk + sl * 32;
+                        float v0[32];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float z0, z1;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[sl][e]), __uint_as_float(sv[sl][e + 1])), cc, nm),
+                                      z0, z1);
+                            v0[e] = fast_exp2(z0);
+                            v0[e + 1] = fast_exp2(z1);
+                        }
+                        if (J0 + 32 > ncol) {
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
-                                if (J0 + e < ncol) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sv[sl][e]));
+                                if (J0 + e >= ncol) v0[e] = 0.f;
                         }
-                        // the chunk's largest scaled logit, unscaled exactly (powers of two)
-                        m = fmaxf(m, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * pow2f(-fq) * fk);
-                    } else {
-                        // exponents as paired FMAs: (s0, s1) * c2 * 2^-(f+e) - mc2, the
-                        // scaled logits times an exact power-of-two correction of the
-                        // constant (an invalid row has mc2 = +inf, so its terms are
-                        // exactly 0); columns past the row are masked only in its
-                        // last, partial chunk
-                        const float c2c = c2q * fk;
-                        const uint64_t cc = f2_pack(c2c, c2c), nm = f2_pack(-mc2, -mc2);
-#pragma unroll
-                        for (int sl = 0; sl < kChunk / 32; ++sl) {
-                            const int J0 = c * kChunk + sl * 32;
-                            float v0[32];
-#pragma unroll
-                            for (int e = 0; e < 32; e += 2) {
-                                float z0, z1;
-                                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[sl][e]), __uint_as_float(sv[sl][e + 1])), cc, nm),
-                                          z0, z1);
-                                v0[e] = fast_exp2(z0);
-                                v0[e + 1] = fast_exp2(z1);
-                            }
-                            if (J0 + 32 > ncol) {
-#pragma unroll
-                                for (int e = 0; e < 32; ++e)
-                                    if (J0 + e >= ncol) v0[e] = 0.f;
-                            }
-                            // lane L now gets the sum of column J0 + L over this warp's 32 rows
-                            const float s0 = transpose_reduce32(v0, lane);
-                            if (J0 + lane < ncol) {
-                                if constexpr (kShared) atomicAdd(my_acc + J0 + lane, s0);
-                                else my_acc[J0 + lane] += s0;
-                            }
+                        // lane L now gets the sum of column J0 + L over this warp's 32 rows
+                        const float s0 = transpose_reduce32(v0, lane);
+                        if (J0 + lane < ncol) {
+                            if constexpr (kShared) atomicAdd(my_acc + J0 + lane, s0);
+                            else my_acc[J0 + lane] += s0;
                         }
                     }
                 }
+                if (has0) {
+                    if (!pull()) { ok = false; break; }
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int sl = 0; sl < kChunk / 32; ++sl) {
+                        const int J0 = c * kChunk + sl * 32;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (J0 + e < ncol) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sv[sl][e]));
+                    }
+                    // the chunk's largest scaled logit, unscaled exactly (powers of two)
+                    m = fmaxf(m, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * fq0 * fk);
+                }
             }
-            if (a.head_union && ok) {
-                // union of heads: this pair's two heads are complete in the
+            if (!ok) break;
+            m_prev = m;
+            fq_prev = fq;
+            if (a.head_union && k >= 1) {
+                // union of heads: pair k - 1's two heads are complete in the
                 // accumulators (four warps each).  Each head's row is normalised by
                 // its own maximum and folded into the output row by maximum; the
                 // accumulators are cleared for the next pair.
+                const int pr = k - 1;
                 const int t = threadIdx.x - 128;
                 const int st = a.acc_stride;
                 auto head_sum = [&](int ww, int J) {
@@ -519,22 +592,22 @@ score_tc_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CU
                 if (!ok) break;
                 float M0 = 0.f, M1 = 0.f;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    M0 = fmaxf(M0, red_h[k]);
-                    M1 = fmaxf(M1, red_h[8 + k]);
+                for (int q = 0; q < 8; ++q) {
+                    M0 = fmaxf(M0, red_h[q]);
+                    M1 = fmaxf(M1, red_h[8 + q]);
                 }
                 const float i0 = 1.f / M0, i1 = h1 ? 1.f / M1 : 0.f;
                 for (int J = t; J < ncol; J += 256) {
                     const float v0 = head_sum(0, J);
-                    float u = v0 == M0 ? 1.f : v0 * i0;
+                    float uu = v0 == M0 ? 1.f : v0 * i0;
                     if (h1) {
                         const float v1 = head_sum(1, J);
-                        u = fmaxf(u, v1 == M1 ? 1.f : v1 * i1);
+                        uu = fmaxf(uu, v1 == M1 ? 1.f : v1 * i1);
                     }
-                    if (pr > 0) u = fmaxf(u, out[J]);
-                    out[J] = u;
+                    if (pr > 0) uu = fmaxf(uu, out[J]);
+                    out[J] = uu;
 #pragma unroll
-                    for (int k = 0; k < (kShared ? 2 : 8); ++k) acc[k * st + J] = 0.f;
+                    for (int q = 0; q < (kShared ? 2 : 8); ++q) acc[q * st + J] = 0.f;
                 }
                 ok = rows_sync(sync_ctr, gen, lane, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
@@ -695,6 +768,22 @@ bool map3(CUtensorMap *m, const void *base, long long n1, long long n2, long lon
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// the queries [tokens][h_q][d] (bf16 or e4m3 codes) as 128-row boxes of one
+// head and 128 bytes of d, 128-byte swizzle
+bool map_queries(CUtensorMap *m, const void *base, int h_q, long long total_q, long long s_head, long long s_tok,
+                 bool fp8) {
+    EncodeTiledFn fn = encode_fn_sc();
+    if (!fn) return false;
+    const int esz = fp8 ? 1 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)h_q, (cuuint64_t)total_q};
+    cuuint64_t strides[2] = {(cuuint64_t)(s_head * esz), (cuuint64_t)(s_tok * esz)};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / esz), 1, 128};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 // rows of each mean term: at least one box of the widest chunk
@@ -704,7 +793,13 @@ int score_tc_rows_pad(const BatchDesc &bd) { return bd.total_kb > 128 ? bd.total
 // column-sum array per row warp (fixed summation order) while it fits, then
 // one per head slot
 static bool score_tc_shared(int max_nkb) { return ScoreCfg<128>::smem_bytes(max_nkb) > 227 * 1024; }
-size_t score_tc_smem_bytes(int max_nkb) { return ScoreCfg<128>::smem_bytes(max_nkb, score_tc_shared(max_nkb)); }
+// query tiles staged by TMA while shared memory has room for them (rows of up
+// to 1072 blocks)
+static bool score_tc_staged(int max_nkb) { return ScoreCfg<128, true>::smem_bytes(max_nkb) <= 227 * 1024; }
+size_t score_tc_smem_bytes(int max_nkb) {
+    if (score_tc_staged(max_nkb)) return ScoreCfg<128, true>::smem_bytes(max_nkb);
+    return ScoreCfg<128>::smem_bytes(max_nkb, score_tc_shared(max_nkb));
+}
 
 cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long long q_stride_tok,
                             long long q_stride_head, const float *q_scale, const float *k_mean, float softmax_scale,
@@ -720,8 +815,8 @@ cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long l
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap tmQ, tmM;
-    (void)q_stride_head;
     const bool shared = score_tc_shared(bd.max_nkb);
+    const bool staged = score_tc_staged(bd.max_nkb);
     if (!map3(&tmM, terms, bd.h_kv, (long long)ScoreCfg<128>::kTerms * rows_pad, kHeadDim,
               (long long)bd.h_kv * kHeadDim, 128))
         return cudaErrorInvalidValue;
@@ -744,10 +839,15 @@ cudaError_t launch_score_tc(const BatchDesc &bd, bool fp8, const void *q, long l
     a.head_union = head_union ? 1 : 0;
     a.status = status;
     a.wait_ns = wait_ns;
-    tmQ = tmM;                           // not read: the row warps load the queries themselves
+    if (staged) {
+        if (!map_queries(&tmQ, q, bd.h_q, bd.total_q, q_stride_head, q_stride_tok, fp8)) return cudaErrorInvalidValue;
+    } else {
+        tmQ = tmM;                       // not read: the row warps load the queries themselves
+    }
     const int smem = (int)score_tc_smem_bytes(bd.max_nkb);
-    auto kern = shared ? (fp8 ? score_tc_kernel<true, 128, true> : score_tc_kernel<false, 128, true>)
-                       : (fp8 ? score_tc_kernel<true, 128, false> : score_tc_kernel<false, 128, false>);
+    auto kern = staged   ? (fp8 ? score_tc_kernel<true, 128, false, true> : score_tc_kernel<false, 128, false, true>)
+                : shared ? (fp8 ? score_tc_kernel<true, 128, true, false> : score_tc_kernel<false, 128, true, false>)
+                         : (fp8 ? score_tc_kernel<true, 128, false, false> : score_tc_kernel<false, 128, false, false>);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<bd.total_rows, kScThreads, smem, st>>>(bd, tmQ, tmM, a);
