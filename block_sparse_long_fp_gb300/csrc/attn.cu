@@ -748,7 +748,6 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             }
             for (int jl = 0; jl < n_items; ++jl, ++it) {
                 const int j = jb + jl;
-                // a bf16 mean tile's key scale, loaded while the S MMA runs
                 const bool got = mbar_wait(bar(BAR_SF + t), it & 1, abort_flag, a.status, a.wait_ns);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }   // tcgen05.ld needs the whole warp
                 tc_fence_after();
