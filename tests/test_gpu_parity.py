@@ -496,6 +496,32 @@ def test_rows_past_the_tensor_core_limit_use_the_fp32_score_kernel(dtype):
     check_scores_and_index(case, g, ref)
 
 
+@pytest.mark.parametrize("nkb", [1072, 1073])
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_rows_at_the_limit_of_the_staged_query_tiles(nkb, dtype):
+    """Rows of up to 1072 blocks stage their query tiles in shared memory (the
+    launch then takes all 227 KB); 1073 reads them from global memory.  Two
+    head pairs, so the phases overlap; sampled score and index rows against
+    the oracle on both sides of the limit."""
+    import oracle
+    import torch
+    from block_sparse_long_fp_gb300 import fprefill
+    spec = synth.Spec("staged-limit", [(nkb * 128, 0)], 4, 1, page_size=128, layout="shuffled", dtype=dtype,
+                      n_needles=2, logit_scale=4.0, config_id=79)
+    case = synth.make_case(spec)
+    rows = np.array([0, 1, 127, 128, 700, nkb - 2, nkb - 1])
+    ref = oracle.discover_and_select(case, row_subset=lambda r, nqb, hkv: rows)
+    layer = fprefill.layer_from_case(case)
+    k_mean, v_mean, score = layer.discover()
+    row_ptr, col_idx, nnz = layer.select(score)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    g = dict(k_mean=k_mean.cpu().numpy(), v_mean=v_mean.cpu().numpy(), score=score.cpu().numpy(),
+             row_ptr=row_ptr.cpu().numpy(), col_idx=col_idx.cpu().numpy())
+    check_pool(case, g, ref)
+    check_scores_and_index(case, g, ref)
+
+
 def _bf16_times_pow2(bits, e):
     """bf16 bit patterns times 2^e, exactly: the exponent field moves by e
     (zeros stay zero; every normal value stays normal)."""
