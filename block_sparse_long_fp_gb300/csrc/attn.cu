@@ -723,12 +723,11 @@ attn_kernel(const __grid_constant__ BatchDesc bd, const __grid_constant__ CUtens
             bool ok = true;
             // logit scale (log2 units): e4m3 codes carry the per-head scales
             const float csc = kFp8 ? a.scale_log2 * __ldg(a.q_scale + head) * __ldg(a.k_scale + U.h) : a.scale_log2;
-            // the running max moves only when it grows by more than kTau (log2
-            // units).  bf16 tolerates weights up to 2^8.  e4m3 stores 256 p: a
-            // row's largest weight stays below 256 * 2^0.5 ~ 362, inside e4m3's
-            // range (448), rounded like every other weight, and small rises of
-            // the max no longer rescale O.
-            constexpr float kTau = kFp8 ? 0.5f : 8.f;
+            // the running max moves only when it grows by more than kTau (bf16
+            // tolerates weights up to 2^8).  For e4m3 it always follows the max, so
+            // the largest weight of a row is exactly 256 = e4m3(256 * 1) and only
+            // the smaller weights carry e4m3 rounding.
+            constexpr float kTau = kFp8 ? 0.f : 8.f;
             const int jb = M.jb;                          // this unit's part: terms jb ..
             // bf16 mean tiles run on fp16 queries (2^f per row) and fp16 key means
             // (2^e per tile); fqr = 2^-f undoes the row's scale.  A part that starts

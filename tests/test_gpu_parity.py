@@ -409,9 +409,10 @@ def test_fp8_attention_sharp_varlen(mean_corr, p_terms):
     MMAs), varlen with a chunk, blocks really skipped.
 
     Queries scaled by 6 make two to four keys dominate each row.  With P as
-    the pages' single e4m3 term of 256 p (p_terms 1) the largest weights
-    carry up to 1/16 relative rounding, which no longer averages out: the
-    measured worst element is 0.062, so that form is held to max-abs 0.1.  With the residual term (p_terms 2,
+    the pages' single e4m3 term of 256 p (p_terms 1) the row's largest
+    weight is exact but the next ones carry up to 1/16 relative rounding,
+    which no longer averages out: the measured worst element is 0.062, so
+    that form is held to max-abs 0.1.  With the residual term (p_terms 2,
     a second PV pass) the weights carry about 1/256 and the FP8 bound
     max-abs 6e-2 holds."""
     from parity_util import FP8_LSE_ABS, FP8_MAX_ABS
