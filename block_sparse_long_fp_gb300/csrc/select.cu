@@ -138,7 +138,10 @@ __device__ __forceinline__ unsigned long long lb_read(const unsigned long long *
 
 constexpr int kRegRow = 1024;      // rows of up to this many blocks decide from registers
 
-__global__ void __launch_bounds__(256)
+// at most 64 registers, so that four CTAs fit on an SM: the 512 CTAs of a
+// 4096-row map then run in one wave (at 128 registers two fit, and the last
+// CTAs started ~9 us late), at the cost of a few spilled bytes
+__global__ void __launch_bounds__(256, 4)
 select_kernel(const __grid_constant__ BatchDesc bd, SelectArgs a, const float *__restrict__ score,
               unsigned long long *__restrict__ lb_state, unsigned epoch, int *__restrict__ row_ptr,
               int *__restrict__ col_idx, long long col_capacity, int *__restrict__ nnz,
